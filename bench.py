@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of the QSA-indexer hot path: paged MQA-logits scoring + top-k.
+
+One step = qsa_paged_mqa_logits + qsa_select_topk over one batch of the
+workload (two kernel launches).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Timing: K steps back to back on one stream between a barrier and a device
+synchronize on both sides, CUDA events around each kernel; inputs and outputs
+rotate over enough copies that their footprint exceeds twice the L2, so no
+step reads another step's data from L2.  `value` is key-cache bytes processed
+per second over the whole step (each request's visible keys counted once),
+summed over ranks with the max time over ranks.  Under torchrun each rank runs
+its own replica of the workload (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qsa_inputs as qi  # noqa: E402
+
+METRIC = "paged index-scoring µs/call and key-cache GB/s vs HBM peak; top-k µs/row"
+DEFAULT_WORKLOAD = "single_row_decode"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------------------
+# Host-side helpers (unit-tested on CPU, including the multi-rank reduction)
+# ---------------------------------------------------------------------------
+
+
+def rank_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+                "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def algorithmic_bytes(spec: qi.Spec):
+    """Bytes each kernel must move at least once per launch."""
+    R, H = spec.num_rows, spec.num_heads
+    pages = int(spec.pages_needed().sum())
+    score = {
+        "keys": spec.key_bytes_touched(),
+        "q": R * H * spec.head_dim * 2,
+        "weights": R * H * 4,
+        "block_table": pages * 4,
+        "visible": R * 4,
+        "logits_out": R * spec.out_cols * 4,
+    }
+    vis = spec.visible.astype(np.int64)
+    topk = {"logits_in": int(np.minimum(vis, spec.out_cols).sum()) * 4, "visible": R * 4,
+            "indices_out": R * spec.k * 4}
+    return score, topk
+
+
+def source_sha(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "rowcore": ["sparse_attention_indexer_02_gb300/csrc/rowcore.cu"],
+    "umma": ["sparse_attention_indexer_02_gb300/csrc/umma.cu"],
+    "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu"],
+}
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since it was captured; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel, {}).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("source_sha") != source_sha(KERNEL_SOURCES[kernel]):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of the SM clock and throttle reasons over a window."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = None
+        self.gpu = gpu_index
+        try:
+            import tempfile
+
+            fd, self.path = tempfile.mkstemp(prefix="qsa_clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        import datetime
+
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, parts))
+        os.unlink(self.path)
+        inside = [p for ts, p in rows if t0 - 0.06 <= ts <= t1 + 0.06] or [p for _, p in rows[-3:]]
+        if not inside:
+            return None
+        sm = [float(p[2]) for p in inside if p[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in inside:
+            for name, v in zip(names, p[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(inside[0][3]) if inside[0][3].replace(".", "").isdigit() else None,
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+
+def oracle_sample_run(inp, requests, threads):
+    """Oracle scoring + top-k for whole requests; returns (seconds, key bytes)."""
+    import oracle
+
+    spec = inp.spec
+    rows = [r for b in requests for r in range(b * spec.rows_per_req, (b + 1) * spec.rows_per_req)]
+    t0 = time.perf_counter()
+    lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
+    oracle.select_topk(lg, spec.visible[rows], spec.k, threads=threads)
+    dt = time.perf_counter() - t0
+    vis = spec.visible.reshape(spec.num_requests, spec.rows_per_req).max(axis=1)
+    key_bytes = int(sum(int(vis[b]) for b in requests)) * spec.key_bytes_per_col
+    return dt, key_bytes, len(rows)
+
+
+def cpu_baseline(inp, budget_s: float = 12.0):
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    spec = inp.spec
+    rng = np.random.default_rng(0)
+    order = rng.permutation(spec.num_requests).tolist()
+    dt1, _, _ = oracle_sample_run(inp, order[:1], threads)  # one request, to size the sample
+    n_req = max(1, min(spec.num_requests, int(budget_s / max(dt1, 1e-6) * 0.8)))
+    # a single request's rows may be many (prefill): cap rows instead
+    if spec.rows_per_req > 64:
+        t_rows = time.perf_counter()
+        sub_rows = [order[0] * spec.rows_per_req + i for i in range(min(64, spec.rows_per_req))]
+        oracle.paged_mqa_logits(inp, rows=sub_rows, threads=threads)
+        per_row = (time.perf_counter() - t_rows) / len(sub_rows)
+        n_rows = max(1, min(spec.rows_per_req, int(budget_s / max(per_row, 1e-9) * 0.8)))
+        rows = sorted(rng.choice(spec.num_rows, n_rows, replace=False).tolist())
+        t0 = time.perf_counter()
+        lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
+        oracle.select_topk(lg, spec.visible[rows], spec.k, threads=threads)
+        dt = time.perf_counter() - t0
+        # keys of a request are shared by its rows: credit each sampled row with
+        # its share of the request's key bytes
+        key_bytes = spec.key_bytes_touched() * len(rows) / spec.num_rows
+        sample = f"{len(rows)} of {spec.num_rows} rows (scoring + top-k), key bytes credited pro rata"
+        return {"value": key_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                "sample": sample, "seconds": dt}
+    dt, kb, nrows = oracle_sample_run(inp, order[:n_req], threads)
+    return {"value": kb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_req} of {spec.num_requests} requests ({nrows} rows, scoring + top-k)",
+            "seconds": dt}
+
+
+def run_reference(args):
+    rank, world, _ = rank_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    threads = oracle.default_threads()
+    spec = qi.WORKLOADS[args.workload]()
+    inp = qi.build_inputs(spec)
+    rng = np.random.default_rng(0)
+    # size each step's sample so the whole run stays within a few minutes
+    dt1, _, _ = oracle_sample_run(inp, [0], threads)
+    budget_step = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    n_req = max(1, min(spec.num_requests, int(budget_step / max(dt1, 1e-6))))
+    steps = []
+    kbytes = 0
+    for i in range(args.warmup + args.steps):
+        reqs = rng.choice(spec.num_requests, n_req, replace=False).tolist()
+        dt, kb, nrows = oracle_sample_run(inp, reqs, threads)
+        if i >= args.warmup:
+            steps.append(dt)
+            kbytes += kb
+    total = sum(steps)
+    value = kbytes / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(spec, None),
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{n_req} of {spec.num_requests} requests per step (scoring + top-k)"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(spec: qi.Spec, l2_note):
+    cfg = {"workload": spec.name, "requests": spec.num_requests, "rows_per_req": spec.rows_per_req,
+           "heads": spec.num_heads, "head_dim": spec.head_dim, "page_cols": spec.page_cols,
+           "out_cols": spec.out_cols, "k": spec.k, "kv": "bf16" if spec.kv_dtype == qi.KV_BF16 else "fp8_e4m3",
+           "visible_cols_total": int(spec.visible.astype(np.int64).sum()),
+           "key_bytes_per_step": spec.key_bytes_touched()}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_indexer_02_gb300 as qsa
+    from sparse_attention_indexer_02_gb300 import build as qbuild
+    from sparse_attention_indexer_02_gb300 import torch_api
+
+    rank, world, local = rank_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qbuild.build()
+    qsa.load_library()
+    if args.variant != "auto":
+        qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA}[args.variant])
+
+    base = qi.WORKLOADS[args.workload]()
+    spec = qi.Spec(base.name, base.num_requests, base.rows_per_req, base.num_heads, base.page_cols,
+                   base.out_cols, base.k, base.kv_dtype, base.visible, base.seed + 7919 * rank,
+                   max_pages=base.max_pages)
+    inp = qi.build_inputs(spec)
+    host = qi.device_tensors(inp, pin=True)
+    R, k = spec.num_rows, spec.k
+
+    # rotation: enough copies that one step's data is out of L2 by its next use
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_copy = inp.kv.nbytes + R * spec.out_cols * 4 + inp.q.nbytes + R * k * 4
+    copies = 1 if args.no_rotate else int(min(16, max(1, math.ceil(2.0 * l2 / per_copy))))
+    sets = []
+    for _ in range(copies):
+        d = {name: t.to(dev, non_blocking=False) for name, t in host.items()}
+        d["out"] = torch.empty((R, spec.out_cols), dtype=torch.float32, device=dev)
+        d["idx"] = torch.empty((R, k), dtype=torch.int32, device=dev)
+        sets.append(d)
+    l2_note = (f"rotating {copies} input/output copies ({copies * per_copy / 1e6:.0f} MB, > 2x the "
+               f"{l2 / 1e6:.0f} MB L2)" if copies > 1 else
+               f"single copy ({per_copy / 1e6:.0f} MB of inputs+outputs, larger than 2x L2)"
+               if per_copy > 2 * l2 else f"single copy ({per_copy / 1e6:.0f} MB), L2 not defeated")
+
+    stream = torch.cuda.current_stream(dev)
+
+    def score(d):
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
+                                   scale_offset=inp.scale_offset, out=d["out"], stream=stream)
+
+    def topk(d):
+        torch_api.select_topk(d["out"], d["visible"], k, out=d["idx"], stream=stream)
+
+    for i in range(args.warmup):
+        d = sets[i % copies]
+        score(d)
+        topk(d)
+    variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
+    time.sleep(0.3 if sampler else 0.0)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(K):
+        d = sets[i % copies]
+        ev[i][0].record(stream)
+        score(d)
+        ev[i][1].record(stream)
+        topk(d)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
+    score_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    topk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    max_ms = max_over_ranks(total_ms)
+    ms_step = max_ms / K
+    key_bytes = spec.key_bytes_touched()
+    value = sum_over_ranks(key_bytes * K) / (max_ms / 1e3) / 1e9
+    score_us = 1e3 * sum(score_ms) / K
+    topk_us = 1e3 * sum(topk_ms) / K
+
+    # roofline of the dominant kernel
+    peaks = measured_peaks()
+    sb, tb = algorithmic_bytes(spec)
+    if score_us >= topk_us:
+        kname, kbytes, kus = variant, sum(sb.values()), score_us
+    else:
+        kname, kbytes, kus = "topk", sum(tb.values()), topk_us
+    achieved = kbytes / (kus * 1e-6) / 1e9
+    traffic = recorded_traffic(kname, spec.name) if kname in KERNEL_SOURCES else None
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes": int(kbytes), "peak_source": f"{peaks['source']} (copy bandwidth)"}
+
+    # end to end through the public API with host buffers: H2D of every input
+    # from pinned memory, both calls, D2H of the top-k indices, every step
+    e2e = None
+    if not args.no_e2e:
+        d = sets[0]
+        out_host = torch.empty((R, k), dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * 4
+        Ke = max(5, min(K, 200))
+        for _ in range(3):
+            for name, t in host.items():
+                d[name].copy_(t, non_blocking=True)
+            score(d)
+            topk(d)
+            out_host.copy_(d["idx"], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            for name, t in host.items():
+                d[name].copy_(t, non_blocking=True)
+            score(d)
+            topk(d)
+            out_host.copy_(d["idx"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = max_over_ranks(e0.elapsed_time(e1))
+        e2e = {"value": sum_over_ranks(key_bytes * Ke) / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms / Ke, "steps": Ke}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == qi.KV_BF16 else "fp8e4m3-keys/bf16-q",
+            "data": "synthetic (seeded; shapes of the pages' workloads)",
+            "config": workload_config(spec, l2_note),
+            "variant": variant,
+            "us_per_call": round(score_us, 3), "key_gbs_scoring": round(key_bytes / (score_us * 1e-6) / 1e9, 1),
+            "topk_us_per_row": round(topk_us / R, 4), "topk_us_per_call": round(topk_us, 3),
+            "step_us": round(1e3 * ms_step, 3),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 2 * K, "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(qi.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--variant", choices=["auto", "rowcore", "umma"], default="auto")
+    ap.add_argument("--no-rotate", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * qsa.h - C ABI of the GB300 (sm_103a) QSA-indexer library: paged MQA-logits
+ * scoring and per-row top-k selection.
+ *
+ * The two compute calls follow the problem statement of the pages:
+ *   - vLLM #62589 "Tile QSA indexer scoring and skip invisible columns",
+ *     Dispatch and Details: qsa_mqa_paged(...) scores request-major query rows
+ *     against a paged compressed-key cache; top_k_per_row_decode reads
+ *     [0, visible_blocks[row]).
+ *   - SGLang #48649 test body: torch_qsa_mqa_decode(q, compressed_cache,
+ *     page_table, context_lens, max_model_len) then
+ *     qsa_fast_topk(logits, row_starts, context_lens, topk).
+ *   - aiter #4221, commit extending fp8_paged_mqa_logits to KVBlockSize>=1:
+ *     the fp8 block-flat cache (KVB e4m3 key rows, then KVB fp32 scales),
+ *     column c of request b at block table[b][c / KVB], slot c % KVB.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *     caller; the library never frees or retains them.  `desc` is host memory,
+ *     read during the call only.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
+ *     enqueued asynchronously; no call synchronises the host with the device,
+ *     so both calls can be captured in a CUDA graph.
+ *   - The library allocates no device memory per call.
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned synchronously (QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED);
+ *     a failed launch returns QSA_ERR_CUDA.  qsa_last_error() describes the
+ *     most recent failure of the calling thread.
+ *   - Device-resident values (page ids, visible counts) are not read by the
+ *     host.  They are clamped on the device (visible to [0, capacity], page ids
+ *     to [0, num_pages)), so bad values give wrong numbers, never a fault.
+ *   - Not thread-safe with respect to qsa_force_variant().
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QSA_ABI_VERSION 1
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or stride */
+  QSA_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. head_dim != 128) */
+  QSA_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
+} qsa_status;
+
+typedef enum qsa_kv_dtype {
+  QSA_KV_BF16 = 0,     /* keys are bf16 [page_cols][head_dim] per page; no scales */
+  QSA_KV_FP8_E4M3 = 1  /* keys are OCP e4m3fn bytes [page_cols][head_dim] per page,
+                          each key dequantised by one fp32 scale (k = e4m3 * scale) */
+} qsa_kv_dtype;
+
+/* Kernel variants the host dispatch chooses between (qsa_plan_variant). */
+typedef enum qsa_variant {
+  QSA_VARIANT_AUTO = -1,
+  QSA_VARIANT_ROWCORE = 0, /* CUDA-core scorer, one row at a time; any shape */
+  QSA_VARIANT_UMMA = 1     /* tcgen05 scorer: 128 keys in M, a request's rows x heads in N */
+} qsa_variant;
+
+/* Shape of one qsa_paged_mqa_logits call.  All sizes are host values. */
+typedef struct qsa_paged_desc {
+  int32_t num_requests;     /* B >= 0                                                  */
+  int32_t rows_per_req;     /* query rows per request, >= 1; rows are request-major:
+                               row r belongs to request r / rows_per_req              */
+  int32_t num_heads;        /* H, 1..64 index heads                                    */
+  int32_t head_dim;         /* D; must be 128 (else QSA_ERR_UNSUPPORTED)               */
+  int32_t page_cols;        /* compressed keys (columns) per page / KV block, >= 1     */
+  int32_t max_pages;        /* entries per block-table row (row stride), >= 1          */
+  int32_t num_pages;        /* pages in the pool; page ids are clamped below this      */
+  int32_t kv_dtype;         /* qsa_kv_dtype                                            */
+  int64_t out_cols;         /* logits row width and row stride (floats), >= 0          */
+  int64_t key_page_stride;  /* bytes between consecutive pages' keys; multiple of 16,
+                               >= page_cols * head_dim * (2 for bf16, 1 for fp8)       */
+  int64_t scale_page_stride;/* fp8: bytes between consecutive pages' scale vectors,
+                               multiple of 4 (block-flat: == key_page_stride); bf16: 0 */
+} qsa_paged_desc;
+
+/*
+ * qsa_paged_mqa_logits - index logits of every query row against its
+ * request's paged keys.
+ *
+ * Defines (ROCm/ATOM #2651 "Changes": per-head ReLU before the heads are
+ * summed; aiter #4221 "Technical details": ReLU then weight; vLLM #62589
+ * first commit: fp32 accumulation), for row r, request b = r / rows_per_req
+ * and column c < out_cols:
+ *
+ *   c >= visible_cols[r]:  out_logits[r*out_cols + c] = -inf
+ *   otherwise:             p = block_table[b*max_pages + c / page_cols],
+ *                          j = c % page_cols,
+ *                          key = K[p][j][:] (bf16), or e4m3(K8[p][j][:]) * scale(p, j),
+ *                          out = sum_h weights[r*H+h] * max(0, dot(q[r][h][:], key))
+ *                          accumulated in fp32 (order unspecified); +0.0 for zero.
+ *
+ * Arguments (device pointers unless stated):
+ *   desc         host; shape as above.
+ *   q            bf16 [R][H][D], R = num_requests * rows_per_req; 16-byte aligned.
+ *   weights      fp32 [R][H] per-row per-head weights (any finite sign).
+ *   kv_cache     key of (page p, slot j) at (char*)kv_cache + p*key_page_stride
+ *                + j*D*esize (esize 2 bf16, 1 fp8); 16-byte aligned.
+ *   scales       fp8: scale of (p, j) at (char*)scales + p*scale_page_stride + 4*j;
+ *                block-flat: scales = (char*)kv_cache + page_cols*D.  bf16: NULL
+ *                (a non-NULL scales with bf16 keys, or NULL with fp8 keys, is
+ *                rejected as mixed operand types, as SGLang #48649's
+ *                rejects_mixed_operand_dtypes test does).
+ *   block_table  int32 [num_requests][max_pages] physical page ids; only the
+ *                entries covering a request's visible columns are read.
+ *   visible_cols int32 [R] visible column count of each row.
+ *   out_logits   fp32 [R][out_cols]; every element is written.
+ *   stream       cudaStream_t.
+ * Returns QSA_OK once the work is enqueued.
+ */
+qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* desc, const void* q, const float* weights,
+                                const void* kv_cache, const float* scales,
+                                const int32_t* block_table, const int32_t* visible_cols,
+                                float* out_logits, void* stream);
+
+/*
+ * qsa_select_topk - per-row top-k column indices of a logits matrix.
+ *
+ * For each row r (vLLM #62589 "Details": top-k reads only [0, visible)):
+ *   n = visible_cols[r] clamped to [0, row_stride];
+ *   n <= k: out_idx[r] = 0, 1, ..., n-1, then -1 in the remaining k - n slots
+ *           (SGLang #48649: rows that fit in top-k select every column);
+ *   n >  k: the k columns that come first in the order (logit descending,
+ *           column ascending); -0.0 and +0.0 compare equal.
+ * The selected columns are written in ascending column order.  NaN logits
+ * inside [0, n) give an unspecified (but in-bounds) selection.
+ *
+ * Arguments (device pointers): logits fp32 rows of row_stride floats;
+ * visible_cols int32 [num_rows]; out_idx int32 [num_rows][k].
+ * num_rows >= 0, row_stride >= 1, 1 <= k <= 2048.
+ */
+qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
+                           const int32_t* visible_cols, int32_t k, int32_t* out_idx,
+                           void* stream);
+
+/*
+ * qsa_plan_variant - host-only dispatch decision for `desc` (no CUDA call).
+ * Writes the qsa_variant qsa_paged_mqa_logits would launch (honouring
+ * qsa_force_variant) to *variant.  Single-row bf16 decode with few heads goes
+ * to the CUDA-core scorer (vLLM #62589 "Dispatch": one-row kernel for
+ * single-row decode, decided from host metadata, no device sync); shapes the
+ * tcgen05 scorer supports go to it; everything else to the CUDA-core scorer.
+ */
+qsa_status qsa_plan_variant(const qsa_paged_desc* desc, int32_t* variant);
+
+/* Force a variant for later calls (QSA_VARIANT_AUTO restores the dispatch).
+ * A forced variant that cannot serve a shape makes the call return
+ * QSA_ERR_UNSUPPORTED.  Meant for tests and A/B measurements. */
+void qsa_force_variant(int32_t variant);
+
+/* Variant launched by this thread's last successful qsa_paged_mqa_logits. */
+int32_t qsa_last_variant(void);
+
+/* Static description of a status code, and of this thread's last failure. */
+const char* qsa_status_string(int32_t status);
+const char* qsa_last_error(void);
+
+/* QSA_ABI_VERSION of the loaded library. */
+int32_t qsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -284,3 +284,29 @@ def gather_rows_for(spec: Spec, max_rows: int, rng: np.random.Generator) -> List
     while len(picks) < max_rows:
         picks.add(int(rng.integers(0, R)))
     return sorted(picks)
+
+
+# ---------------------------------------------------------------------------
+# Host -> device copies (plumbing only).
+# ---------------------------------------------------------------------------
+
+
+def device_tensors(inp: Inputs, device="cuda", pin: bool = False) -> dict:
+    """torch tensors of ``inp`` on ``device`` (or pinned host memory with pin=True).
+
+    q is bf16 [R, H, D]; kv is the raw paged cache as uint8 [num_pages, stride];
+    scales (fp8 only) is a view at the block-flat scale offset."""
+    import torch
+
+    def t(a):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return x.pin_memory() if pin else x.to(device)
+
+    d = {
+        "q": t(inp.q.view(np.int16)).view(torch.bfloat16),
+        "weights": t(inp.weights),
+        "kv": t(inp.kv),
+        "block_table": t(inp.block_table),
+        "visible": t(inp.spec.visible),
+    }
+    return d

@@ -1,0 +1,146 @@
+"""ctypes binding of libqsa.so (include/qsa.h): argument marshalling only.
+
+Every step of scoring and selection runs in the library's CUDA kernels; this
+module converts torch tensors (or raw integer addresses) to pointers, fills
+the descriptor struct and raises on a non-OK status.  If the library is not
+built the import of a call fails loudly - there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqsa.so")
+
+QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
+KV_BF16, KV_FP8_E4M3 = 0, 1
+VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA = -1, 0, 1
+VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma"}
+
+# Every symbol include/qsa.h declares.
+EXPORTED = ("qsa_paged_mqa_logits", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+            "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version")
+
+
+class QSAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+class PagedDesc(ctypes.Structure):
+    _fields_ = [
+        ("num_requests", ctypes.c_int32),
+        ("rows_per_req", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("page_cols", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("out_cols", ctypes.c_int64),
+        ("key_page_stride", ctypes.c_int64),
+        ("scale_page_stride", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+
+def load_library():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is not built: run `python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        lib.qsa_paged_mqa_logits.restype = ctypes.c_int
+        lib.qsa_paged_mqa_logits.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_select_topk.restype = ctypes.c_int
+        lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
+        lib.qsa_plan_variant.restype = ctypes.c_int
+        lib.qsa_plan_variant.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(i32)]
+        lib.qsa_force_variant.restype = None
+        lib.qsa_force_variant.argtypes = [i32]
+        lib.qsa_last_variant.restype = i32
+        lib.qsa_last_variant.argtypes = []
+        lib.qsa_status_string.restype = ctypes.c_char_p
+        lib.qsa_status_string.argtypes = [i32]
+        lib.qsa_last_error.restype = ctypes.c_char_p
+        lib.qsa_last_error.argtypes = []
+        lib.qsa_abi_version.restype = i32
+        lib.qsa_abi_version.argtypes = []
+        _lib = lib
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return load_library().qsa_status_string(int(st)).decode()
+
+
+def last_error() -> str:
+    return load_library().qsa_last_error().decode()
+
+
+def _addr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int):
+    if st != QSA_OK:
+        raise QSAError(st, last_error())
+
+
+def make_desc(num_requests, rows_per_req, num_heads, page_cols, max_pages, num_pages, out_cols,
+              key_page_stride, kv_dtype=KV_BF16, scale_page_stride=0, head_dim=128) -> PagedDesc:
+    return PagedDesc(int(num_requests), int(rows_per_req), int(num_heads), int(head_dim), int(page_cols),
+                     int(max_pages), int(num_pages), int(kv_dtype), int(out_cols), int(key_page_stride),
+                     int(scale_page_stride))
+
+
+def paged_mqa_logits(desc: PagedDesc, q, weights, kv_cache, scales, block_table, visible_cols,
+                     out_logits, stream=None) -> None:
+    st = load_library().qsa_paged_mqa_logits(ctypes.byref(desc), _addr(q), _addr(weights), _addr(kv_cache),
+                                             _addr(scales), _addr(block_table), _addr(visible_cols),
+                                             _addr(out_logits), _stream(stream))
+    _check(st)
+
+
+def select_topk(logits, num_rows: int, row_stride: int, visible_cols, k: int, out_idx, stream=None) -> None:
+    st = load_library().qsa_select_topk(_addr(logits), int(num_rows), int(row_stride), _addr(visible_cols),
+                                        int(k), _addr(out_idx), _stream(stream))
+    _check(st)
+
+
+def plan_variant(desc: PagedDesc) -> int:
+    v = ctypes.c_int32(-1)
+    _check(load_library().qsa_plan_variant(ctypes.byref(desc), ctypes.byref(v)))
+    return v.value
+
+
+def force_variant(v: int) -> None:
+    load_library().qsa_force_variant(int(v))
+
+
+def last_variant() -> int:
+    return load_library().qsa_last_variant()
+
+
+def abi_version() -> int:
+    return load_library().qsa_abi_version()

@@ -1,0 +1,37 @@
+// Device helpers shared by the scoring and top-k kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qsa {
+
+// bf16 pair packed in a 32-bit word -> two fp32 values (exact: bf16 is the top
+// half of a binary32).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ReLU that keeps NaN (a poisoned key stays visible), like torch.relu.
+__device__ __forceinline__ float relu_keep_nan(float x) { return x < 0.0f ? 0.0f : x; }
+
+// Order-preserving map of fp32 to uint32 for a descending top-k: a larger
+// float gives a larger key; -0.0 is folded onto +0.0 first.
+__device__ __forceinline__ uint32_t topk_key(float x) {
+  uint32_t u = __float_as_uint(x + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi) {
+  return v < lo ? lo : (v > hi ? hi : v);
+}
+
+// 16-byte read-only global load that bypasses L1 allocation (streamed keys).
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+}  // namespace qsa

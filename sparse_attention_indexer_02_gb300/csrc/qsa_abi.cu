@@ -1,0 +1,203 @@
+// C ABI entry points: host-side validation, variant dispatch and launches.
+// Declarations, argument meaning and error behaviour are in include/qsa.h.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "qsa_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+thread_local int32_t g_last_variant = -1;
+std::atomic<int32_t> g_forced_variant{QSA_VARIANT_AUTO};
+
+qsa_status fail(qsa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+qsa_status validate_desc(const qsa_paged_desc* d) {
+  if (!d) return fail(QSA_ERR_INVALID_ARG, "desc is NULL");
+  if (d->num_requests < 0) return fail(QSA_ERR_INVALID_ARG, "num_requests < 0");
+  if (d->rows_per_req < 1) return fail(QSA_ERR_INVALID_ARG, "rows_per_req < 1");
+  if (d->num_heads < 1) return fail(QSA_ERR_INVALID_ARG, "num_heads < 1");
+  if (d->num_heads > 64) return fail(QSA_ERR_UNSUPPORTED, "num_heads > 64");
+  if (d->head_dim != 128) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", d->head_dim);
+  if (d->page_cols < 1) return fail(QSA_ERR_INVALID_ARG, "page_cols < 1");
+  if (d->max_pages < 1) return fail(QSA_ERR_INVALID_ARG, "max_pages < 1");
+  if (d->num_pages < 1) return fail(QSA_ERR_INVALID_ARG, "num_pages < 1");
+  if (d->out_cols < 0) return fail(QSA_ERR_INVALID_ARG, "out_cols < 0");
+  if (d->kv_dtype != QSA_KV_BF16 && d->kv_dtype != QSA_KV_FP8_E4M3)
+    return fail(QSA_ERR_INVALID_ARG, "unknown kv_dtype %d", d->kv_dtype);
+  const int64_t rows = (int64_t)d->num_requests * d->rows_per_req;
+  if (rows > 0x7FFFFFFFLL) return fail(QSA_ERR_INVALID_ARG, "num_requests * rows_per_req overflows int32");
+  const int64_t esize = d->kv_dtype == QSA_KV_BF16 ? 2 : 1;
+  const int64_t key_bytes = (int64_t)d->page_cols * d->head_dim * esize;
+  if (d->key_page_stride % 16 != 0 || d->key_page_stride < key_bytes)
+    return fail(QSA_ERR_INVALID_ARG, "key_page_stride must be a multiple of 16 and >= %lld",
+                (long long)key_bytes);
+  if (d->kv_dtype == QSA_KV_FP8_E4M3 &&
+      (d->scale_page_stride % 4 != 0 || d->scale_page_stride < 4LL * d->page_cols))
+    return fail(QSA_ERR_INVALID_ARG, "scale_page_stride must be a multiple of 4 and >= 4 * page_cols");
+  return QSA_OK;
+}
+
+}  // namespace
+
+namespace qsa {
+
+cudaError_t device_info(DeviceInfo* info) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && have[dev]) {
+    *info = cache[dev];
+    return cudaSuccess;
+  }
+  DeviceInfo d{dev, 0, 0};
+  e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) {
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *info = d;
+  return cudaSuccess;
+}
+
+}  // namespace qsa
+
+extern "C" {
+
+int32_t qsa_abi_version(void) { return QSA_ABI_VERSION; }
+
+const char* qsa_status_string(int32_t s) {
+  switch (s) {
+    case QSA_OK: return "QSA_OK";
+    case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+    case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+    case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+    default: return "unknown qsa_status";
+  }
+}
+
+const char* qsa_last_error(void) { return g_last_error; }
+
+void qsa_force_variant(int32_t v) { g_forced_variant.store(v); }
+
+int32_t qsa_last_variant(void) { return g_last_variant; }
+
+qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) {
+  qsa_status st = validate_desc(d);
+  if (st != QSA_OK) return st;
+  if (!variant) return fail(QSA_ERR_INVALID_ARG, "variant is NULL");
+  const int32_t forced = g_forced_variant.load();
+  const char* why = nullptr;
+  if (forced == QSA_VARIANT_ROWCORE) {
+    *variant = QSA_VARIANT_ROWCORE;
+  } else if (forced == QSA_VARIANT_UMMA) {
+    if (!qsa::umma_supports(*d, &why))
+      return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant cannot serve this shape: %s", why);
+    *variant = QSA_VARIANT_UMMA;
+  } else if (d->rows_per_req == 1 && d->kv_dtype == QSA_KV_BF16 && d->num_heads <= 8) {
+    // single-row bf16 decode with few heads: the CUDA-core one-row scorer
+    *variant = QSA_VARIANT_ROWCORE;
+  } else if (qsa::umma_supports(*d, &why)) {
+    *variant = QSA_VARIANT_UMMA;
+  } else {
+    *variant = QSA_VARIANT_ROWCORE;
+  }
+  return QSA_OK;
+}
+
+qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const float* weights,
+                                const void* kv_cache, const float* scales,
+                                const int32_t* block_table, const int32_t* visible_cols,
+                                float* out_logits, void* stream) {
+  qsa_status st = validate_desc(d);
+  if (st != QSA_OK) return st;
+  const int64_t rows = (int64_t)d->num_requests * d->rows_per_req;
+  const bool fp8 = d->kv_dtype == QSA_KV_FP8_E4M3;
+  if (fp8 && !scales) return fail(QSA_ERR_INVALID_ARG, "fp8 keys need a scales pointer");
+  if (!fp8 && scales) return fail(QSA_ERR_INVALID_ARG, "bf16 keys take no scales (mixed operand types)");
+  if (rows == 0 || d->out_cols == 0) {
+    g_last_variant = -1;
+    return QSA_OK;
+  }
+  if (!q || !weights || !kv_cache || !block_table || !visible_cols || !out_logits)
+    return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(q, 16) || !aligned(kv_cache, 16))
+    return fail(QSA_ERR_INVALID_ARG, "q and kv_cache must be 16-byte aligned");
+  if (!aligned(weights, 4) || !aligned(block_table, 4) || !aligned(visible_cols, 4) ||
+      !aligned(out_logits, 4) || (fp8 && !aligned(scales, 4)))
+    return fail(QSA_ERR_INVALID_ARG, "weights, block_table, visible_cols, out_logits, scales must be 4-byte aligned");
+  int32_t variant = 0;
+  st = qsa_plan_variant(d, &variant);
+  if (st != QSA_OK) return st;
+
+  qsa::ScoreParams p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.weights = weights;
+  p.kv = static_cast<const uint8_t*>(kv_cache);
+  p.scales = reinterpret_cast<const uint8_t*>(scales);
+  p.block_table = block_table;
+  p.visible = visible_cols;
+  p.out = out_logits;
+  p.out_cols = d->out_cols;
+  p.key_page_stride = d->key_page_stride;
+  p.scale_page_stride = fp8 ? d->scale_page_stride : 0;
+  const int64_t cap = (int64_t)d->max_pages * d->page_cols;
+  p.capacity = cap < d->out_cols ? cap : d->out_cols;
+  p.num_requests = d->num_requests;
+  p.rows_per_req = d->rows_per_req;
+  p.num_rows = (int32_t)rows;
+  p.num_heads = d->num_heads;
+  p.page_cols = d->page_cols;
+  p.max_pages = d->max_pages;
+  p.num_pages = d->num_pages;
+  p.fp8 = fp8 ? 1 : 0;
+
+  const char* msg = "launch failed";
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = variant == QSA_VARIANT_UMMA ? qsa::launch_umma(p, s, &msg)
+                                              : qsa::launch_rowcore(p, s, &msg);
+  if (e == cudaErrorInvalidValue && msg && strcmp(msg, "launch failed") != 0)
+    return fail(QSA_ERR_UNSUPPORTED, "%s", msg);
+  if (e != cudaSuccess)
+    return fail(QSA_ERR_CUDA, "scoring launch (variant %d): %s", variant, cudaGetErrorString(e));
+  g_last_variant = variant;
+  return QSA_OK;
+}
+
+qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
+                           const int32_t* visible_cols, int32_t k, int32_t* out_idx, void* stream) {
+  if (num_rows < 0) return fail(QSA_ERR_INVALID_ARG, "num_rows < 0");
+  if (row_stride < 1) return fail(QSA_ERR_INVALID_ARG, "row_stride < 1");
+  if (k < 1 || k > 2048) return fail(QSA_ERR_INVALID_ARG, "k must be in 1..2048 (got %d)", k);
+  if (num_rows > 0x7FFFFFFFLL) return fail(QSA_ERR_INVALID_ARG, "num_rows exceeds 2^31 - 1");
+  if (num_rows == 0) return QSA_OK;
+  if (!logits || !visible_cols || !out_idx) return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (!aligned(logits, 4) || !aligned(visible_cols, 4) || !aligned(out_idx, 4))
+    return fail(QSA_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, k, out_idx,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
+  return QSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,44 @@
+// Internal declarations shared by the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+// Parameters of one scoring launch, resolved on the host from qsa_paged_desc.
+struct ScoreParams {
+  const uint16_t* q;        // bf16 bits [R][H][128]
+  const float* weights;     // [R][H]
+  const uint8_t* kv;        // paged keys
+  const uint8_t* scales;    // fp8 scales base (NULL for bf16)
+  const int32_t* block_table;
+  const int32_t* visible;
+  float* out;
+  int64_t out_cols;
+  int64_t key_page_stride;
+  int64_t scale_page_stride;
+  int64_t capacity;         // min(out_cols, max_pages * page_cols): largest legal visible count
+  int32_t num_requests, rows_per_req, num_rows, num_heads, page_cols, max_pages, num_pages;
+  int32_t fp8;
+};
+
+// Each launcher returns cudaSuccess or the launch error; `msg` gets a reason
+// when a shape is rejected (then the return is cudaErrorInvalidValue).
+cudaError_t launch_rowcore(const ScoreParams& p, cudaStream_t stream, const char** msg);
+bool umma_supports(const qsa_paged_desc& d, const char** why);
+cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg);
+cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride,
+                        const int32_t* visible, int32_t k, int32_t* out, cudaStream_t stream);
+
+// Cached per-device properties (queried once per device).
+struct DeviceInfo {
+  int device;
+  int num_sms;
+  int max_smem_optin;
+};
+cudaError_t device_info(DeviceInfo* info);
+
+}  // namespace qsa

@@ -1,0 +1,54 @@
+"""torch-tensor form of the two C-ABI calls (argument marshalling only).
+
+The descriptor is read off the tensors' shapes and strides; every byte of the
+result is computed by libqsa.so.  All tensors must be on the current CUDA
+device; work is enqueued on the current torch stream unless one is given.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _abi
+
+
+def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Tensor,
+                     block_table: torch.Tensor, visible_cols: torch.Tensor, *, page_cols: int,
+                     out_cols: int, kv_dtype: int = _abi.KV_BF16, scale_offset: int = -1,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Index logits fp32 [R, out_cols] (include/qsa.h, qsa_paged_mqa_logits).
+
+    q: bf16 [R, H, 128]; weights: fp32 [R, H]; kv_cache: [num_pages, ...] paged
+    keys whose dim-0 stride is the page stride; block_table: int32
+    [num_requests, max_pages]; visible_cols: int32 [R].  For fp8 keys in the
+    block-flat layout pass kv_dtype=KV_FP8_E4M3 and the byte offset of the
+    scales inside a block (page_cols * 128)."""
+    R, H, D = q.shape
+    B, max_pages = block_table.shape
+    if B == 0 or R % B:
+        raise ValueError("rows must be a whole number of rows per request")
+    page_stride = kv_cache.stride(0) * kv_cache.element_size()
+    if out is None:
+        out = torch.empty((R, out_cols), dtype=torch.float32, device=q.device)
+    scales = None
+    scale_stride = 0
+    if kv_dtype == _abi.KV_FP8_E4M3:
+        if scale_offset < 0:
+            raise ValueError("fp8 keys need the scale offset inside a block")
+        scales = kv_cache.data_ptr() + scale_offset
+        scale_stride = page_stride
+    desc = _abi.make_desc(B, R // B, H, page_cols, max_pages, kv_cache.shape[0], out_cols, page_stride,
+                          kv_dtype=kv_dtype, scale_page_stride=scale_stride, head_dim=D)
+    _abi.paged_mqa_logits(desc, q, weights, kv_cache, scales, block_table, visible_cols, out, stream)
+    return out
+
+
+def select_topk(logits: torch.Tensor, visible_cols: torch.Tensor, k: int,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Top-k column indices int32 [rows, k] (include/qsa.h, qsa_select_topk)."""
+    rows = logits.shape[0]
+    if out is None:
+        out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
+    _abi.select_topk(logits, rows, logits.stride(0), visible_cols, k, out, stream)
+    return out

@@ -1,0 +1,134 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+symbol include/qsa.h declares, and its host-side validation and dispatch
+behave.  No call here reaches a kernel launch: every compute call below is
+rejected by host validation before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_indexer_02_gb300 as qsa
+from sparse_attention_indexer_02_gb300 import build as qbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qbuild.build()
+    return qsa.load_library()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in qsa.h but not exported"
+    assert set(names) == set(qsa.EXPORTED)
+
+
+def test_abi_version_and_status_strings(lib):
+    assert qsa.abi_version() == 1
+    assert qsa.status_string(qsa.QSA_OK) == "QSA_OK"
+    assert qsa.status_string(qsa.QSA_ERR_UNSUPPORTED) == "QSA_ERR_UNSUPPORTED"
+    assert "unknown" in qsa.status_string(99)
+
+
+def _desc(**kw):
+    base = dict(num_requests=2, rows_per_req=4, num_heads=4, page_cols=16, max_pages=8, num_pages=16,
+                out_cols=128, key_page_stride=16 * 128 * 2)
+    base.update(kw)
+    return qsa.make_desc(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), qsa.QSA_ERR_UNSUPPORTED),
+    (dict(num_heads=65), qsa.QSA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), qsa.QSA_ERR_INVALID_ARG),
+    (dict(rows_per_req=0), qsa.QSA_ERR_INVALID_ARG),
+    (dict(num_requests=-1), qsa.QSA_ERR_INVALID_ARG),
+    (dict(page_cols=0), qsa.QSA_ERR_INVALID_ARG),
+    (dict(out_cols=-5), qsa.QSA_ERR_INVALID_ARG),
+    (dict(key_page_stride=16 * 128 * 2 - 16), qsa.QSA_ERR_INVALID_ARG),
+    (dict(key_page_stride=16 * 128 * 2 + 8), qsa.QSA_ERR_INVALID_ARG),
+    (dict(kv_dtype=7), qsa.QSA_ERR_INVALID_ARG),
+    (dict(kv_dtype=qsa.KV_FP8_E4M3, key_page_stride=16 * 132, scale_page_stride=2), qsa.QSA_ERR_INVALID_ARG),
+])
+def test_descriptor_validation(lib, kw, status):
+    d = _desc(**kw)
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.plan_variant(d)
+    assert e.value.status == status
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.paged_mqa_logits(d, None, None, None, None, None, None, None, stream=0)
+    assert e.value.status == status
+
+
+def test_mixed_operand_types_rejected(lib):
+    """SGLang #48649 test list: rejects_mixed_operand_dtypes."""
+    with pytest.raises(qsa.QSAError) as e:  # bf16 keys with a scales pointer
+        qsa.paged_mqa_logits(_desc(), 16, 16, 16, 16, 16, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "mixed" in str(e.value)
+    d8 = _desc(kv_dtype=qsa.KV_FP8_E4M3, key_page_stride=16 * 132, scale_page_stride=16 * 132)
+    with pytest.raises(qsa.QSAError) as e:  # fp8 keys without scales
+        qsa.paged_mqa_logits(d8, 16, 16, 16, None, 16, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.paged_mqa_logits(_desc(), None, 16, 16, None, 16, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+    with pytest.raises(qsa.QSAError) as e:  # q not 16-byte aligned
+        qsa.paged_mqa_logits(_desc(), 24, 16, 16, None, 16, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+    with pytest.raises(qsa.QSAError) as e:  # out not 4-byte aligned
+        qsa.paged_mqa_logits(_desc(), 16, 16, 16, None, 16, 16, 18, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_empty_calls_are_no_ops(lib):
+    qsa.paged_mqa_logits(_desc(num_requests=0), None, None, None, None, None, None, None, stream=0)
+    qsa.paged_mqa_logits(_desc(out_cols=0), None, None, None, None, None, None, None, stream=0)
+    qsa.select_topk(None, 0, 10, None, 8, None, stream=0)
+
+
+@pytest.mark.parametrize("k", [0, -1, 2049])
+def test_topk_k_range(lib, k):
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.select_topk(16, 4, 100, 16, k, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_topk_argument_checks(lib):
+    for args in [(16, -1, 100, 16, 8, 16), (16, 4, 0, 16, 8, 16), (None, 4, 100, 16, 8, 16),
+                 (18, 4, 100, 16, 8, 16)]:
+        with pytest.raises(qsa.QSAError) as e:
+            qsa.select_topk(*args, stream=0)
+        assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+
+
+def test_last_error_names_the_problem(lib):
+    with pytest.raises(qsa.QSAError):
+        qsa.plan_variant(_desc(head_dim=96))
+    assert "head_dim" in qsa.last_error()
+
+
+def test_dispatch_decisions(lib):
+    """Host dispatch on host metadata only (vLLM #62589 'Dispatch')."""
+    qsa.force_variant(qsa.VARIANT_AUTO)
+    # single-row bf16 decode with 4 heads -> CUDA-core one-row scorer
+    assert qsa.plan_variant(_desc(rows_per_req=1)) == qsa.VARIANT_ROWCORE
+    # odd page size: only the CUDA-core scorer serves it
+    assert qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256)) == qsa.VARIANT_ROWCORE
+    qsa.force_variant(qsa.VARIANT_ROWCORE)
+    assert qsa.plan_variant(_desc()) == qsa.VARIANT_ROWCORE
+    qsa.force_variant(qsa.VARIANT_AUTO)

@@ -1,0 +1,298 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Every case uses the seeded generator, a NaN-prefilled output buffer and a
+NaN poison page behind every unused block-table entry.  Logits are compared
+element by element (tolerances in qsa_testlib); the -inf mask is bit-exact;
+top-k is bit-exact against the oracle's top-k of the same GPU logits, and
+within tie tolerance against the oracle's own logits.
+"""
+import numpy as np
+import pytest
+
+import qsa_inputs as qi
+from qsa_testlib import (assert_logits_match, assert_topk_strict, assert_topk_within_tie_tolerance,
+                         exact_case, nan_filled)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import sparse_attention_indexer_02_gb300 as qsa  # noqa: E402
+from sparse_attention_indexer_02_gb300 import torch_api  # noqa: E402
+
+VARIANTS = {"auto": qsa.VARIANT_AUTO, "rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    qsa.load_library()
+    yield
+    qsa.force_variant(qsa.VARIANT_AUTO)
+
+
+def desc_of(inp):
+    s = inp.spec
+    stride = inp.key_page_stride
+    return qsa.make_desc(s.num_requests, s.rows_per_req, s.num_heads, s.page_cols, s.max_pages,
+                         inp.num_pages, s.out_cols, stride, kv_dtype=s.kv_dtype,
+                         scale_page_stride=stride if s.kv_dtype == qi.KV_FP8 else 0)
+
+
+def supported(inp, variant):
+    qsa.force_variant(variant)
+    try:
+        qsa.plan_variant(desc_of(inp))
+        return True
+    except qsa.QSAError as e:
+        if e.status == qsa.QSA_ERR_UNSUPPORTED:
+            return False
+        raise
+    finally:
+        qsa.force_variant(qsa.VARIANT_AUTO)
+
+
+def gpu_logits(inp, variant=qsa.VARIANT_AUTO, dev=None, stream=None):
+    s = inp.spec
+    d = dev if dev is not None else qi.device_tensors(inp)
+    out = nan_filled((s.num_rows, s.out_cols), torch.float32, "cuda")
+    qsa.force_variant(variant)
+    try:
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=s.page_cols, out_cols=s.out_cols, kv_dtype=s.kv_dtype,
+                                   scale_offset=inp.scale_offset, out=out, stream=stream)
+        ran = qsa.last_variant()
+    finally:
+        qsa.force_variant(qsa.VARIANT_AUTO)
+    torch.cuda.synchronize()
+    return out, ran, d
+
+
+def gpu_topk(logits_t, visible_t, k):
+    idx = nan_filled((logits_t.shape[0], k), torch.int32, "cuda")
+    torch_api.select_topk(logits_t, visible_t, k, out=idx)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy()
+
+
+# (name, B, rows/req, H, page_cols, visible list (cycled), out_cols, k)
+SMALL = [
+    ("grid_6_100_700_p64", 3, 1, 4, 64, [6, 100, 700], 704, 64),  # SGLang decode_grid_covers_every_group
+    ("mtp4_multi_tile_ragged", 2, 4, 4, 16, [1000, 1001, 1002, 1003, 300, 301, 302, 303], 1100, 256),
+    ("mtp4_p64", 3, 4, 4, 64, [517, 518, 518, 519, 64, 65, 65, 66, 129, 130, 130, 131], 576, 100),
+    ("single_row_h4_p16", 5, 1, 4, 16, [33, 129, 0, 640, 257], 640, 32),
+    ("single_row_h1", 2, 1, 1, 16, [200, 77], 256, 16),
+    ("h2_rows3", 2, 3, 2, 16, [150, 151, 152, 40, 41, 42], 160, 20),
+    ("h3_odd_page5", 2, 2, 3, 5, [61, 62, 13, 14], 70, 10),
+    ("h8_rows2_p32", 2, 2, 8, 32, [300, 301, 129, 130], 320, 50),
+    ("h16_rows4", 2, 4, 16, 16, [270, 271, 272, 273, 5, 6, 7, 8], 288, 64),
+    ("h64_single_row", 2, 1, 64, 64, [400, 257], 448, 64),
+    ("rows16_p64", 1, 16, 4, 64, list(range(300, 316)), 320, 128),
+    ("rows64_prefill_like", 1, 80, 4, 64, [200 + i // 4 for i in range(80)], 256, 64),
+    ("visible_full_and_empty", 3, 2, 4, 16, [96, 96, 0, 0, 95, 1], 96, 8),
+    ("page128_single", 2, 2, 4, 128, [700, 701, 129, 128], 768, 100),
+]
+
+
+def small_spec(case, kv_dtype, seed=123):
+    name, B, rpr, H, pc, vis, oc, k = case
+    R = B * rpr
+    v = (vis * R)[:R]
+    return qi.custom(name, B, rpr, H, pc, v, oc, k=k, kv_dtype=kv_dtype, seed=seed)
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("case", SMALL, ids=[c[0] for c in SMALL])
+def test_small_shapes_match_oracle(oracle_mod, case, kv_dtype, variant):
+    if kv_dtype == qi.KV_FP8 and (case[4] * 132) % 16:
+        pytest.skip("a block-flat fp8 page of this size is not 16-byte aligned")
+    inp = qi.build_inputs(small_spec(case, kv_dtype))
+    if not supported(inp, VARIANTS[variant]):
+        pytest.skip(f"{variant} does not serve this shape")
+    out, ran, d = gpu_logits(inp, VARIANTS[variant])
+    if variant != "auto":
+        assert ran == VARIANTS[variant]
+    g = out.cpu().numpy()
+    ref = oracle_mod.paged_mqa_logits(inp)
+    assert_logits_match(g, ref, kv_dtype, where=f"{case[0]}/{variant}")
+    k = inp.spec.k
+    idx = gpu_topk(out, d["visible"], k)
+    assert_topk_strict(idx, oracle_mod.select_topk(g, inp.spec.visible, k), where=case[0])
+    assert_topk_within_tie_tolerance(idx, ref, inp.spec.visible, k, kv_dtype, where=case[0])
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
+def test_exact_integer_inputs_are_bit_exact(oracle_mod, kv_dtype, variant):
+    """Integer q/keys and power-of-two weights/scales: fp32 is exact in any order."""
+    spec = qi.custom("exact_gpu", 2, 4, 4, 16, [300, 301, 302, 303, 17, 18, 19, 0], 320, kv_dtype=kv_dtype,
+                     seed=4)
+    inp, _, _, _ = exact_case(kv_dtype, spec)
+    if not supported(inp, VARIANTS[variant]):
+        pytest.skip(f"{variant} does not serve this shape")
+    out, _, _ = gpu_logits(inp, VARIANTS[variant])
+    ref = oracle_mod.paged_mqa_logits(inp)
+    assert (out.cpu().numpy().view(np.uint32) == ref.view(np.uint32)).all()
+
+
+def test_variants_agree_with_each_other(oracle_mod):
+    inp = qi.build_inputs(small_spec(SMALL[1], qi.KV_BF16))
+    a, _, d = gpu_logits(inp, qsa.VARIANT_ROWCORE)
+    if not supported(inp, qsa.VARIANT_UMMA):
+        pytest.skip("tcgen05 scorer does not serve this shape")
+    b, _, _ = gpu_logits(inp, qsa.VARIANT_UMMA, dev=d)
+    assert_logits_match(b.cpu().numpy(), a.cpu().numpy(), qi.KV_BF16, where="umma vs rowcore")
+
+
+def test_repeat_calls_are_bit_identical():
+    inp = qi.build_inputs(small_spec(SMALL[2], qi.KV_BF16))
+    a, _, d = gpu_logits(inp)
+    b, _, _ = gpu_logits(inp, dev=d)
+    assert (a.cpu().numpy().view(np.uint32) == b.cpu().numpy().view(np.uint32)).all()
+    ia = gpu_topk(a, d["visible"], 100)
+    ib = gpu_topk(b, d["visible"], 100)
+    assert (ia == ib).all()
+
+
+def test_side_stream(oracle_mod):
+    inp = qi.build_inputs(small_spec(SMALL[3], qi.KV_BF16))
+    s = torch.cuda.Stream()
+    d = qi.device_tensors(inp)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        out, _, _ = gpu_logits(inp, dev=d, stream=s)
+    assert_logits_match(out.cpu().numpy(), oracle_mod.paged_mqa_logits(inp), qi.KV_BF16)
+
+
+def test_cuda_graph_capture_and_replay(oracle_mod):
+    """vLLM #62589 Validation: capture, then replay with new queries and lengths written in place."""
+    spec = small_spec(SMALL[1], qi.KV_BF16)
+    inp = qi.build_inputs(spec)
+    d = qi.device_tensors(inp)
+    s = inp.spec
+    out = torch.empty((s.num_rows, s.out_cols), dtype=torch.float32, device="cuda")
+    idx = torch.empty((s.num_rows, s.k), dtype=torch.int32, device="cuda")
+
+    def step():
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=s.page_cols, out_cols=s.out_cols, out=out)
+        torch_api.select_topk(out, d["visible"], s.k, out=idx)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm-up outside capture (first-call setup)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    # new queries and shorter lengths, written in place
+    rng = np.random.default_rng(99)
+    new_q = qi._bf16_bits(rng.standard_normal(inp.q.shape, dtype=np.float32))
+    new_vis = np.maximum(spec.visible - rng.integers(0, 200, size=spec.visible.shape), 0).astype(np.int32)
+    d["q"].copy_(torch.from_numpy(new_q.view(np.int16)).view(torch.bfloat16))
+    d["visible"].copy_(torch.from_numpy(new_vis))
+    out.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    inp.q = new_q
+    ref = oracle_mod.paged_mqa_logits(inp, visible=new_vis)
+    got = out.cpu().numpy()
+    assert_logits_match(got, ref, qi.KV_BF16, where="graph replay")
+    assert_topk_strict(idx.cpu().numpy(), oracle_mod.select_topk(got, new_vis, s.k))
+
+
+# --------------------------------------------------------------------------
+# Top-k kernel on its own
+# --------------------------------------------------------------------------
+
+
+def _topk_case(rows, width, vis, k, zero_frac=0.06, seed=0):
+    rng = np.random.default_rng(seed)
+    x = qi.random_logit_rows(rng, rows, width, vis, zero_frac)
+    return x
+
+
+@pytest.mark.parametrize("k", [1, 7, 256, 2048])
+def test_topk_edge_rows(oracle_mod, k):
+    vis = [0, 1, k - 1 if k > 1 else 0, k, k + 1, 3 * k + 5, 4000, 9000]
+    width = max(vis) + 3
+    x = _topk_case(len(vis), width, vis, k, zero_frac=0.2, seed=k)
+    # a row of all-equal values and a row mixing -0.0 and +0.0
+    x[6, :4000] = 1.25
+    x[7, :9000:2] = -0.0
+    x[7, 1:9000:2] = 0.0
+    xt = torch.from_numpy(x).cuda()
+    vt = torch.tensor(vis, dtype=torch.int32, device="cuda")
+    idx = gpu_topk(xt, vt, k)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, np.array(vis, np.int32), k))
+    for r, n in enumerate(vis):
+        if n <= k:
+            assert idx[r].tolist() == list(range(n)) + [-1] * (k - n)
+
+
+def test_topk_rows_longer_than_the_shared_memory_cache(oracle_mod):
+    vis = [65537, 60000, 49153, 49152]
+    x = _topk_case(4, 65600, vis, 2048, seed=5)
+    xt = torch.from_numpy(x).cuda()
+    vt = torch.tensor(vis, dtype=torch.int32, device="cuda")
+    idx = gpu_topk(xt, vt, 2048)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, np.array(vis, np.int32), 2048))
+
+
+def test_topk_threshold_ties_take_the_lowest_columns(oracle_mod):
+    # 3000 exact zeros around the k-th place: the lowest-column zeros must win
+    x = np.zeros((2, 5000), np.float32)
+    x[:, 4000:] = 2.0
+    x[1, ::7] = 0.5
+    vis = np.array([5000, 4999], np.int32)
+    xt = torch.from_numpy(x).cuda()
+    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 1500)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 1500))
+
+
+def test_topk_visible_beyond_stride_is_clamped():
+    x = np.arange(40, dtype=np.float32).reshape(2, 20)
+    xt = torch.from_numpy(x).cuda()
+    vt = torch.tensor([1000, -5], dtype=torch.int32, device="cuda")
+    idx = gpu_topk(xt, vt, 4)
+    assert sorted(idx[0].tolist()) == [16, 17, 18, 19]
+    assert idx[1].tolist() == [-1, -1, -1, -1]
+
+
+# --------------------------------------------------------------------------
+# Full-size workloads in the bench launch configuration (auto dispatch),
+# checked on sampled rows (logits) and on every row (top-k vs oracle top-k
+# of the same logits).
+# --------------------------------------------------------------------------
+
+FULL = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "fp8_h64", "prefill_chunk",
+        "mtp3_large_p64"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload_sampled(oracle_mod, name):
+    spec = qi.WORKLOADS[name]()
+    inp = qi.build_inputs(spec)
+    out, ran, d = gpu_logits(inp)
+    rows = qi.gather_rows_for(spec, 6 if spec.num_heads > 4 else 12, np.random.default_rng(1))
+    ref = oracle_mod.paged_mqa_logits(inp, rows=rows)
+    sub = out[torch.tensor(rows, device="cuda")].cpu().numpy()
+    assert_logits_match(sub, ref, spec.kv_dtype, where=f"{name} rows {rows}")
+    idx_t = nan_filled((spec.num_rows, spec.k), torch.int32, "cuda")
+    torch_api.select_topk(out, d["visible"], spec.k, out=idx_t)
+    torch.cuda.synchronize()
+    idx = idx_t.cpu().numpy()
+    # strict top-k on a bounded set of rows (the oracle sorts each row)
+    trows = rows if spec.num_rows > 512 else list(range(spec.num_rows))
+    g_rows = out[torch.tensor(trows, device="cuda")].cpu().numpy()
+    assert_topk_strict(idx[trows], oracle_mod.select_topk(g_rows, spec.visible[trows], spec.k), where=name)
+    assert_topk_within_tie_tolerance(idx[rows], ref, spec.visible[rows], spec.k, spec.kv_dtype, where=name)
+    # every masked entry of every row, bit-exact
+    vis_t = d["visible"].long()
+    cols = torch.arange(spec.out_cols, device="cuda")
+    masked = cols[None, :] >= vis_t[:, None]
+    bits = out.view(torch.int32)
+    assert bool((bits[masked] == np.int32(np.uint32(0xFF800000).view(np.int32))).all())
+    assert not bool(torch.isnan(out[~masked]).any())

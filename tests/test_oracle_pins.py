@@ -16,6 +16,7 @@ import torch
 
 import qsa_inputs as qi
 from oracle import brute
+from qsa_testlib import exact_case as _exact_case, int_bf16 as _int_bf16
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -123,34 +124,6 @@ def test_logits_match_numpy_bruteforce(oracle_mod, d, kv_dtype):
     got = oracle_mod.paged_mqa_logits(inp)
     ref = brute.logits(inp)
     assert _close_1ulp(got, ref)
-
-
-def _int_bf16(vals):
-    return qi._bf16_bits(np.asarray(vals, dtype=np.float32))
-
-
-def _exact_case(kv_dtype):
-    """q, keys in {-3..3}; weights and scales powers of two: every partial sum is an
-    integer multiple of a power of two below 2^24, so the result is exact."""
-    rng = np.random.default_rng(5)
-    spec = qi.custom("exact", 2, 2, 3, 8, [19, 20, 5, 24], 24, kv_dtype=kv_dtype, seed=3)
-    inp = qi.build_inputs(spec)
-    qv = rng.integers(-3, 4, size=inp.q.shape)
-    inp.q = _int_bf16(qv)
-    inp.weights = rng.choice(np.array([0.25, 0.5, 1.0, 2.0], dtype=np.float32), size=inp.weights.shape)
-    D, pc = spec.head_dim, spec.page_cols
-    kvals = rng.integers(-3, 4, size=(inp.num_pages, pc, D))
-    if kv_dtype == qi.KV_BF16:
-        inp.kv = _int_bf16(kvals.reshape(inp.num_pages, -1)).view(np.uint8).reshape(inp.num_pages, -1).copy()
-        scales = np.ones((inp.num_pages, pc))
-    else:
-        codes = qi._e4m3_codes(kvals.astype(np.float32)).reshape(inp.num_pages, pc * D)
-        scales = rng.choice(np.array([0.5, 1.0, 2.0], dtype=np.float32), size=(inp.num_pages, pc))
-        kv = np.empty((inp.num_pages, pc * (D + 4)), dtype=np.uint8)
-        kv[:, : pc * D] = codes
-        kv[:, pc * D:] = scales.astype(np.float32).view(np.uint8).reshape(inp.num_pages, pc * 4)
-        inp.kv = kv
-    return inp, qv, kvals, scales
 
 
 @pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
