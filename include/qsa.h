@@ -161,6 +161,15 @@ int32_t qsa_last_variant(void);
 const char* qsa_status_string(int32_t status);
 const char* qsa_last_error(void);
 
+/*
+ * qsa_device_status - the library's device fault word.  Non-zero (bit 0) after
+ * a scoring kernel gave up waiting on one of its internal barriers (about one
+ * second): that launch left its output incomplete and returned early instead
+ * of hanging the GPU.  Synchronises the current device, then writes the word
+ * to *flags (host pointer) and clears it when `clear` is non-zero.
+ */
+qsa_status qsa_device_status(uint32_t* flags, int32_t clear);
+
 /* QSA_ABI_VERSION of the loaded library. */
 int32_t qsa_abi_version(void);
 

@@ -21,7 +21,7 @@ VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma"}
 
 # Every symbol include/qsa.h declares.
 EXPORTED = ("qsa_paged_mqa_logits", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
-            "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version")
+            "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
 class QSAError(RuntimeError):
@@ -72,6 +72,8 @@ def load_library():
         lib.qsa_last_error.argtypes = []
         lib.qsa_abi_version.restype = i32
         lib.qsa_abi_version.argtypes = []
+        lib.qsa_device_status.restype = ctypes.c_int
+        lib.qsa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         _lib = lib
     return _lib
 
@@ -140,6 +142,13 @@ def force_variant(v: int) -> None:
 
 def last_variant() -> int:
     return load_library().qsa_last_variant()
+
+
+def device_status(clear: bool = True) -> int:
+    """Device fault word (non-zero: a kernel gave up on a barrier wait); synchronises."""
+    v = ctypes.c_uint32(0)
+    _check(load_library().qsa_device_status(ctypes.byref(v), 1 if clear else 0))
+    return v.value
 
 
 def abi_version() -> int:

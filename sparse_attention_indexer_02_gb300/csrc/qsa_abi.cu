@@ -184,6 +184,13 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const fl
   return QSA_OK;
 }
 
+qsa_status qsa_device_status(uint32_t* flags, int32_t clear) {
+  if (!flags) return fail(QSA_ERR_INVALID_ARG, "flags is NULL");
+  cudaError_t e = qsa::read_fault_word(flags, clear != 0);
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "reading the device fault word: %s", cudaGetErrorString(e));
+  return QSA_OK;
+}
+
 qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
                            const int32_t* visible_cols, int32_t k, int32_t* out_idx, void* stream) {
   if (num_rows < 0) return fail(QSA_ERR_INVALID_ARG, "num_rows < 0");

@@ -57,7 +57,12 @@ def assert_logits_match(gpu: np.ndarray, ref: np.ndarray, kv_dtype: int, where: 
 
 def assert_topk_strict(gpu_idx: np.ndarray, oracle_idx: np.ndarray, where: str = ""):
     """Same logits in, same index set out, bit for bit (both sides ascending)."""
-    g = np.sort(np.asarray(gpu_idx), axis=1)
+    # both sides list the set in ascending column order with -1 padding last;
+    # sort anyway (unused slots last) so only the set is compared
+    big = np.iinfo(np.int32).max
+    g = np.asarray(gpu_idx).astype(np.int64)
+    g = np.sort(np.where(g < 0, big, g), axis=1)
+    g = np.where(g == big, -1, g)
     o = np.asarray(oracle_idx)
     bad = (g != o).any(axis=1)
     assert not bad.any(), f"{where}: top-k differs in rows {np.flatnonzero(bad)[:8].tolist()}"

@@ -296,3 +296,8 @@ def test_full_size_workload_sampled(oracle_mod, name):
     bits = out.view(torch.int32)
     assert bool((bits[masked] == np.int32(np.uint32(0xFF800000).view(np.int32))).all())
     assert not bool(torch.isnan(out[~masked]).any())
+
+
+def test_no_kernel_gave_up_on_a_barrier():
+    """Every bounded wait above completed: the device fault word is still clear."""
+    assert qsa.device_status(clear=True) == 0
