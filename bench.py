@@ -122,7 +122,7 @@ def source_sha(paths):
 
 KERNEL_SOURCES = {
     "rowcore": ["sparse_attention_indexer_02_gb300/csrc/rowcore.cu"],
-    "umma": ["sparse_attention_indexer_02_gb300/csrc/umma.cu"],
+    "umma": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
     "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu"],
 }
 

@@ -10,6 +10,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import resource
 import shutil
 import subprocess
 import sys
@@ -47,11 +48,27 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+def _raise_stack_limit():
+    # the compiler recurses deeply on large unrolled kernels: give it the hard stack limit
+    soft, hard = resource.getrlimit(resource.RLIMIT_STACK)
+    try:
+        resource.setrlimit(resource.RLIMIT_STACK, (hard, hard))
+    except (ValueError, OSError):
+        pass
+
+
 def _compile(src: str) -> str:
     unit = os.path.splitext(os.path.basename(src))[0]
     obj = os.path.join(BUILD, unit + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
-    res = subprocess.run(cmd, capture_output=True, text=True)
+    res = subprocess.run(cmd, capture_output=True, text=True, preexec_fn=_raise_stack_limit)
+    if res.returncode in (139, -11) or "Segmentation fault" in res.stderr:
+        # the compiler itself crashed (seen with ptxas 13.0 on aarch64 hosts):
+        # rebuild this unit without ptxas optimisation rather than fail the build
+        sys.stderr.write(f"WARNING: the CUDA compiler crashed on {unit}.cu; rebuilding it with "
+                         f"-Xptxas -O0 (correct but slower code)\n")
+        res = subprocess.run(cmd[:-3] + ["-Xptxas", "-O0"] + cmd[-3:], capture_output=True, text=True,
+                             preexec_fn=_raise_stack_limit)
     with open(os.path.join(BUILD, f"ptxas_{unit}.log"), "w") as f:
         f.write(res.stdout + res.stderr)
     if res.returncode != 0:

@@ -14,6 +14,14 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // ReLU that keeps NaN (a poisoned key stays visible), like torch.relu.
 __device__ __forceinline__ float relu_keep_nan(float x) { return x < 0.0f ? 0.0f : x; }
 
+// max(x, 0) in one instruction that returns NaN for a NaN input (max.NaN),
+// so a poisoned key is not hidden by the ReLU.
+__device__ __forceinline__ float relu_nan(float x) {
+  float r;
+  asm("max.NaN.f32 %0, %1, 0f00000000;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // Order-preserving map of fp32 to uint32 for a descending top-k: a larger
 // float gives a larger key; -0.0 is folded onto +0.0 first.
 __device__ __forceinline__ uint32_t topk_key(float x) {

@@ -1,0 +1,13 @@
+// tcgen05 scorer instantiations for bf16 keys (see umma_kernel.cuh).
+#include "umma_kernel.cuh"
+
+namespace qsa {
+namespace umma {
+
+cudaError_t launch_bf16(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                        const Layout& L, int grid, cudaStream_t s) {
+  return launch_any<false>(heads, kv, qm, up, L, grid, s);
+}
+
+}  // namespace umma
+}  // namespace qsa

@@ -1,0 +1,631 @@
+// tcgen05 scorer: 128 keys in M, a request's rows x heads in N.
+//
+// The pages stack a request's rows x heads into the M dimension of one MFMA
+// so a key tile is read once for all of them (ROCm/ATOM #2651 "Changes":
+// BMT rows x heads = one 16-row tile, per-head ReLU before the head sum).  On
+// sm_100-class tensor cores M is 128 wide, so here the roles swap: each tile
+// of 128 consecutive key columns is the A operand (M = 128 lanes of TMEM, one
+// key per lane) and the group's rows x heads are the B operand (N = 16..256,
+// zero or don't-care padded).  The epilogue then owns one key per thread and
+// reduces heads in registers, and its stores of one row are 32 consecutive
+// floats per warp.
+//
+// Structure (one persistent CTA per SM, 10 warps):
+//  * schedule: every CTA derives, from the visible counts, the tile count of
+//    each row group (tiles past the group's widest visible column are never
+//    scheduled - the early exit of vLLM #62589 "Overview") and takes an equal
+//    contiguous share of the flattened (group, tile) list, plus an equal share
+//    of the pure -inf tail (columns past each group's last tile).
+//  * warp 0 (TMA): per tile, lanes fetch the block-table entries of the tile's
+//    pages and each issues the page's two 64-column K-halves as 3-D tensor
+//    copies into a 128-byte-swizzled stage (aiter #4221 KVBlockSize>=1 commit:
+//    block = table[b][col / page_cols], slot = col % page_cols).  A new group's
+//    q is loaded by a 2-D tensor copy once the previous group's MMAs are done.
+//  * warp 1 (MMA): one thread issues 8 tcgen05.mma (K = 16 each) per tile into
+//    one of two TMEM accumulators and commits the stage back to the producer.
+//  * warps 2-9 (epilogue, two warps per TMEM lane quadrant, each taking
+//    alternate row blocks of the group): tcgen05.ld of the tile's columns,
+//    per head ReLU * weight, head sum, +0.0, -inf past the row's visible
+//    count, store.
+// Every barrier wait gives up after about a second, sets the device fault
+// word (qsa_device_status) and lets the CTA drain and exit.
+#pragma once
+#include <cuda.h>
+
+#include "device_common.cuh"
+#include "qsa_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace qsa {
+namespace umma {
+
+constexpr int kBM = 128;                    // keys per tile (MMA M)
+constexpr int kHalfBytes = kBM * 128;       // one 64-element K-half of a bf16 key tile
+constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB
+constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
+constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
+// Warp roles: 0 TMA, 1 MMA, then the epilogue warps (two per TMEM lane
+// quadrant for bf16 keys, one for fp8), then 8 fp8->bf16 converter warps
+// (fp8) or 4 spare warps that only take part in the CTA-wide barriers (bf16:
+// ptxas 13.0 for aarch64 hosts crashes on this kernel without them).
+template <bool FP8>
+struct Roles {
+  static constexpr int kEpiWarps = FP8 ? 4 : 8;
+  static constexpr int kEpiThreads = 32 * kEpiWarps;
+  static constexpr int kConvWarps = FP8 ? 8 : 4;
+  static constexpr int kConvThreads = 32 * kConvWarps;
+  static constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
+};
+constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr int kMaxSmem = 232448;                 // 227 KB opt-in limit per CTA
+
+
+struct UmmaParams {
+  unsigned int* fault;    // device fault word: bit 0 set when a bounded wait gives up
+  const uint8_t* scales;  // fp8: scale of (page, slot) at scales + page * scale_stride + 4 * slot
+  int64_t scale_stride;
+  const float* weights;
+  const int32_t* block_table;
+  const int32_t* visible;
+  float* out;
+  int64_t out_cols;
+  int64_t capacity;
+  int32_t num_rows, rows_per_req, num_heads, page_cols, max_pages, num_pages;
+  int32_t group_rows, groups_per_req, num_groups, tiles_cap, box_rows;
+  int32_t stream_out;  // logits far larger than L2: write them with evict-first stores
+  int32_t keep_keys;   // several row groups reuse each key tile: keep keys in L2
+};
+
+// Shared-memory layout of one CTA (byte offsets from a 1024-aligned base);
+// computed on the host and passed in, so N and the stage count are runtime.
+struct Layout {
+  int32_t n;            // MMA N (rows x heads of a group, padded to 16..256)
+  int32_t stages;       // TMA stages in flight (bf16 key tiles, or fp8 key tiles)
+  int32_t stage_bytes;  // 32 KB (bf16 tile) or 16 KB (fp8 tile)
+  int32_t a_stages;     // fp8: bf16 operand stages written by the converter; bf16: 0
+  int32_t tmem_cols;    // 2 accumulators of N columns, power of two >= 32
+  uint32_t idesc;       // tcgen05 instruction descriptor for M = 128, this N
+  int32_t a_off, b_off, bar_off, misc_off, epi_off, sched_off, total;
+};
+
+inline Layout make_layout(int N, int groups, bool fp8) {
+  Layout L;
+  L.n = N;
+  L.tmem_cols = 2 * N < 32 ? 32 : 2 * N;
+  L.idesc = ptx::idesc_bf16_f32(kBM, N);
+  L.stage_bytes = fp8 ? kFp8StageBytes : kTileBytes;
+  L.a_stages = fp8 ? kFp8ConvStages : 0;
+  const int tail = N * 256 + (2 * 8 + 2 * kFp8ConvStages + 7) * 8 + 32 + 2 * 256 * 4 + 8 * (groups + 1);
+  int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
+  L.stages = st > 8 ? 8 : st;
+  L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
+  L.b_off = L.a_off + L.a_stages * kTileBytes;
+  L.bar_off = L.b_off + N * 256;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + 2 + 2 + 3;
+  L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
+  L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
+  L.sched_off = L.epi_off + 2 * 256 * 4;        // pref[G + 1], gmax[G]
+  L.total = 1024 + L.sched_off + 8 * (groups + 1);
+  return L;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on abort or time-out.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned int* fault) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kSpinCycles) {
+      *abort_flag = 1;
+      atomicOr(fault, 1u);
+      return false;
+    }
+  }
+}
+
+// Largest g with pref[g] <= t (pref is non-decreasing, pref[0] = 0).
+__device__ __forceinline__ int find_group(const int32_t* pref, int num_groups, int t) {
+  int lo = 0, hi = num_groups;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ void epi_bar(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Two fp8 e4m3 codes (bytes 0 and 1, or 2 and 3, of w) -> bf16x2, exactly.
+// The code's 7 magnitude bits placed at bf16 bits 10..4 give a bf16 with
+// exponent field eeee and fraction mmm0000, i.e. 2^(e-127) * 1.mmm (or the
+// subnormal 2^-126 * 0.mmm); one exact multiply by 2^120 rebiases it to the
+// e4m3 value 2^(e-7) * 1.mmm (or 2^-6 * 0.mmm).  The NaN codes S.1111.111 are
+// not inputs of this path.
+template <int HI>
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
+  const uint32_t t = __byte_perm(w, 0u, HI ? 0x4342u : 0x4140u);  // code0 -> bits 0..7, code1 -> bits 16..23
+  const uint32_t bits = ((t & 0x00800080u) << 8) | ((t & 0x007F007Fu) << 4);
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));  // 2^120 in both halves
+  return r;
+}
+
+template <int H, bool FP8>
+__global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
+    umma_score_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                      const UmmaParams p, const Layout L) {
+  using R = Roles<FP8>;
+  constexpr int kThreads = R::kThreads;
+  constexpr int kEpiThreads = R::kEpiThreads;
+  extern __shared__ uint8_t smem_raw[];
+  const int N = L.n;
+  const int kStages = L.stages;
+  const int kAStages = L.a_stages;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* S = smem;                          // TMA stages
+  uint8_t* A = FP8 ? smem + L.a_off : smem;   // MMA A-operand stages (bf16, 128-byte swizzle)
+  uint8_t* Bq = smem + L.b_off;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* empty = full + kStages;
+  uint64_t* afull = empty + kStages;          // fp8: converter -> MMA
+  uint64_t* aempty = afull + kAStages;        // fp8: MMA -> converter
+  uint64_t* tfull = aempty + kAStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* qfull = tempty + 2;
+  uint64_t* qempty = qfull + 1;
+  uint64_t* mma_done = qempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.misc_off + 4);
+  float* w_s = reinterpret_cast<float*>(smem + L.epi_off);
+  int32_t* vis_s = reinterpret_cast<int32_t*>(w_s + 256);
+  int32_t* pref = reinterpret_cast<int32_t*>(smem + L.sched_off);
+  int32_t* gmax = pref + p.num_groups + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.num_groups;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], FP8 ? R::kConvThreads : 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      ptx::mbar_init(&afull[s], R::kConvThreads);
+      ptx::mbar_init(&aempty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], kEpiThreads);
+    }
+    ptx::mbar_init(qfull, 1);
+    ptx::mbar_init(qempty, 1);
+    ptx::mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&kv_map);
+    ptx::prefetch_tmap(&q_map);
+  }
+  // Per-group tile counts from the visible counts (device data, no host sync).
+  for (int g = threadIdx.x; g < G; g += kThreads) {
+    const int b = g / p.groups_per_req, j = g % p.groups_per_req;
+    const int r0 = b * p.rows_per_req + j * p.group_rows;
+    const int nr = min(p.group_rows, p.rows_per_req - j * p.group_rows);
+    int64_t mv = 0;
+    for (int i = 0; i < nr; ++i) {
+      const int64_t v = clamp64(p.visible[r0 + i], 0, p.capacity);
+      mv = v > mv ? v : mv;
+    }
+    gmax[g] = (int32_t)mv;
+    pref[g] = (int32_t)((mv + kBM - 1) / kBM);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (warp == 0) {  // exclusive scan of the tile counts, total in pref[G]
+    const int per = (G + 31) / 32;
+    const int lo = min(G, lane * per), hi = min(G, lo + per);
+    int s = 0;
+    for (int i = lo; i < hi; ++i) s += pref[i];
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - s;
+    for (int i = lo; i < hi; ++i) {
+      const int t = pref[i];
+      pref[i] = run;
+      run += t;
+    }
+    if (lane == 31) pref[G] = incl;
+  }
+  __syncthreads();
+  const int total = pref[G];
+  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    const uint64_t policy = p.keep_keys ? ptx::policy_evict_last() : ptx::policy_evict_first();
+    const int pc = p.page_cols;
+    const int bpt = pc >= kBM ? 1 : kBM / pc;  // boxes (pages) per full tile, <= 16
+    const int tiles_per_batch = 32 / bpt;       // one box per lane per batch
+    const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // per K-half (bf16) or per page (fp8)
+    const uint32_t copies = FP8 ? 1u : 2u;
+    // Page id of this lane's box in the batch starting at tile tb (-1: none).
+    // Lane l covers tile tb + l / bpt, box l % bpt.
+    auto lane_page = [&](int tb) -> int32_t {
+      const int tl = tb + lane / bpt, box = lane % bpt;
+      if (tl >= t_end) return -1;
+      const int gl = find_group(pref, G, tl);
+      const int c0 = (tl - pref[gl]) * kBM;
+      const int lim = gmax[gl] - c0;
+      const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
+      if (box >= nbox) return -1;
+      const int64_t lp = (int64_t)c0 / pc + (pc >= kBM ? 0 : box);
+      const int32_t v = __ldg(p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp);
+      return v < 0 ? 0 : (v >= p.num_pages ? p.num_pages - 1 : v);
+    };
+    int stage = 0;
+    uint32_t phase = 0;
+    int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
+    int qg = -1;
+    uint32_t q_loads = 0;
+    uint32_t filled_mask = 0, last_phase_bits = 0;
+    bool ok = true;
+    int32_t cur = t_begin < t_end ? lane_page(t_begin) : -1;
+    for (int tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
+      // the next batch's block-table entries load while this batch is issued
+      const int32_t nxt = lane_page(tb + tiles_per_batch);
+      for (int i = 0; i < tiles_per_batch && tb + i < t_end; ++i) {
+        const int t = tb + i;
+        while (t >= pref[g + 1]) ++g;
+        const int b = g / p.groups_per_req, jj = g % p.groups_per_req;
+        const int r0 = b * p.rows_per_req + jj * p.group_rows;
+        const int c0 = (t - pref[g]) * kBM;
+        const int lim = gmax[g] - c0;  // visible columns in this tile (>= 1)
+        const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
+        if (g != qg) {
+          if (q_loads > 0) ok = wait_phase(qempty, (q_loads - 1) & 1, abort_flag, p.fault);
+          if (!ok) break;
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(qfull, 2u * N * 128u);
+            ptx::tma_load_2d(Bq, &q_map, 0, r0 * H, qfull);
+            ptx::tma_load_2d(Bq + N * 128, &q_map, 64, r0 * H, qfull);
+          }
+          qg = g;
+          ++q_loads;
+        }
+        ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, p.fault);
+        if (!ok) break;
+        if (lane == 0) ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes);
+        __syncwarp();
+        if (lane / bpt == i && cur >= 0) {
+          const int box = lane % bpt;
+          const int y = pc >= kBM ? c0 % pc : 0;
+          uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * 128u;
+          ptx::tma_load_3d(dst, &kv_map, 0, y, cur, &full[stage], policy);
+          if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, cur, &full[stage], policy);
+        }
+        filled_mask |= 1u << stage;
+        last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      cur = nxt;
+    }
+    // Drain: every copy this warp issued has landed before the CTA tears down.
+    if (lane == 0 && *abort_flag) {
+      for (int s = 0; s < kStages; ++s)
+        if (filled_mask & (1u << s)) {
+          const long long t0 = clock64();
+          while (!ptx::mbar_try_wait(&full[s], (last_phase_bits >> s) & 1u) && clock64() - t0 < kSpinCycles) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
+      int qg = -1;
+      uint32_t q_uses = 0;
+      const uint32_t a_base = ptx::smem_u32(A);
+      const uint32_t b_base = ptx::smem_u32(Bq);
+      bool ok = true;
+      for (int t = t_begin; t < t_end && ok; ++t) {
+        while (t >= pref[g + 1]) ++g;
+        if (g != qg) {
+          if (qg >= 0) ptx::mma_commit(qempty);  // q buffer free once earlier MMAs finish
+          ok = wait_phase(qfull, q_uses & 1u, abort_flag, p.fault);
+          if (!ok) break;
+          ++q_uses;
+          qg = g;
+        }
+        ok = wait_phase(&tempty[acc], acc_phase ^ 1u, abort_flag, p.fault);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        ok = wait_phase(FP8 ? &afull[stage] : &full[stage], phase, abort_flag, p.fault);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * N);
+        const uint32_t a0 = a_base + stage * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (uint32_t)(k & 3) * 32u;
+          const uint64_t ad = ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff);
+          const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
+          ptx::mma_bf16(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(FP8 ? &aempty[stage] : &empty[stage]);
+        ptx::mma_commit(&tfull[acc]);
+        if (++stage == (FP8 ? kAStages : kStages)) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // every MMA issued above has completed before TMEM is released
+      ptx::mma_commit(mma_done);
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinCycles) {
+      }
+    }
+    __syncwarp();
+  } else if (warp < 2 + R::kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    constexpr int kHalves = R::kEpiWarps / 4;  // warps sharing one TMEM lane quadrant
+    const int et = threadIdx.x - 64;           // 0 .. kEpiThreads - 1
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2;          // which of the quadrant's warps
+    const int m = quad * 32 + lane;            // key row of the tile = TMEM lane
+    const int64_t oc = p.out_cols;
+
+    // (1) this CTA's share of the -inf tail.  Group g's tail is its tiles
+    // [T_g, tiles_cap), i.e. columns [T_g * 128, out_cols) of its rows; the
+    // CTA takes a contiguous slice of the tail tiles of all groups and writes
+    // each group's part of it as a plain row-by-row range (16-byte streaming
+    // stores when rows are 16-byte aligned).
+    {
+      const int64_t Tc = p.tiles_cap;
+      const int64_t F = (int64_t)G * Tc - total;
+      int64_t f = F * blockIdx.x / gridDim.x;
+      const int64_t f1 = F * (blockIdx.x + 1) / gridDim.x;
+      if (f < f1) {
+        // fill prefix fp(g) = g * Tc - pref[g] is non-decreasing; find the group of f
+        int lo = 0, hi = G;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if ((int64_t)mid * Tc - pref[mid] <= f) lo = mid;
+          else hi = mid;
+        }
+        const bool vec = (oc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+        const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int g = lo; f < f1 && g < G; ++g) {
+          const int64_t fpg = (int64_t)g * Tc - pref[g];
+          const int Tg = pref[g + 1] - pref[g];
+          const int64_t fe = min(f1, fpg + (Tc - Tg));
+          if (f >= fe) continue;
+          const int64_t ca = (Tg + (f - fpg)) * kBM;
+          const int64_t cb = min((Tg + (fe - fpg)) * kBM, oc);
+          f = fe;
+          if (ca >= cb) continue;
+          const int jj = g % p.groups_per_req;
+          const int64_t r0 = (int64_t)(g / p.groups_per_req) * p.rows_per_req + jj * p.group_rows;
+          const int nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+          for (int j = 0; j < nr; ++j) {
+            float* o = p.out + (r0 + j) * oc;
+            if (vec) {
+              for (int64_t cc = ca + 4 * et; cc < cb; cc += 4 * kEpiThreads)
+                __stcs(reinterpret_cast<float4*>(o + cc), ninf4);
+            } else {
+              for (int64_t cc = ca + et; cc < cb; cc += kEpiThreads) __stcs(o + cc, -INFINITY);
+            }
+          }
+        }
+      }
+    }
+
+    // (2) computed tiles.  Column n of the accumulator is (row n / H, head
+    // n % H).  A "unit" is the smallest run of 16-column TMEM loads that holds
+    // whole rows: one load (16 / H rows) for H <= 16, H / 16 loads (one row)
+    // for H > 16.  The warps of a quadrant take alternate units.
+    constexpr int kRowsPerUnit = H >= 16 ? 1 : 16 / H;
+    constexpr int kLdPerUnit = H >= 16 ? H / 16 : 1;
+    constexpr int kUnitsPerBatch = 4 / kLdPerUnit;  // four loads in flight
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
+    int eg = -1, r0 = 0, nr = 0, b = 0;
+    bool ok = true;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      while (t >= pref[g + 1]) ++g;
+      if (g != eg) {
+        epi_bar(kEpiThreads);
+        b = g / p.groups_per_req;
+        const int jj = g % p.groups_per_req;
+        r0 = b * p.rows_per_req + jj * p.group_rows;
+        nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+        for (int i = et; i < nr * H; i += kEpiThreads) w_s[i] = p.weights[(int64_t)r0 * H + i];
+        for (int i = et; i < nr; i += kEpiThreads) vis_s[i] = (int32_t)clamp64(p.visible[r0 + i], 0, p.capacity);
+        epi_bar(kEpiThreads);
+        eg = g;
+      }
+      const int64_t c = (int64_t)(t - pref[g]) * kBM + m;
+      // fp8: this key's dequantisation scale.  relu(s x) = |s| relu(sign(s) x)
+      // for every s, so the sign goes inside the ReLU and |s| is applied once
+      // per row after the head sum.
+      float sgn = 1.0f, mag = 1.0f;
+      if (FP8) {
+        float sc = 0.0f;
+        if (c < gmax[g]) {
+          const int32_t v = __ldg(p.block_table + (int64_t)b * p.max_pages + c / p.page_cols);
+          const int32_t pg = v < 0 ? 0 : (v >= p.num_pages ? p.num_pages - 1 : v);
+          sc = __ldg(reinterpret_cast<const float*>(p.scales + (int64_t)pg * p.scale_stride +
+                                                    4 * (c % p.page_cols)));
+        }
+        sgn = sc < 0.0f ? -1.0f : 1.0f;
+        mag = fabsf(sc);
+      }
+      ok = wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
+      float* const ob = p.out + (int64_t)r0 * oc + c;  // row r0, this key's column
+      const int nunits = H >= 16 ? nr : (nr + kRowsPerUnit - 1) / kRowsPerUnit;
+      for (int u0 = half; u0 < nunits; u0 += kHalves * kUnitsPerBatch) {
+        uint32_t v[4][16];
+#pragma unroll
+        for (int q = 0; q < kUnitsPerBatch; ++q)
+          if (u0 + kHalves * q < nunits)
+#pragma unroll
+            for (int l = 0; l < kLdPerUnit; ++l)
+              ptx::tmem_ld16(tb + (uint32_t)(16 * ((u0 + kHalves * q) * kLdPerUnit + l)), v[q * kLdPerUnit + l]);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < kUnitsPerBatch; ++q) {
+          const int u = u0 + kHalves * q;
+          if (u >= nunits) break;
+#pragma unroll
+          for (int rr = 0; rr < kRowsPerUnit; ++rr) {
+            const int j = u * kRowsPerUnit + rr;
+            if (j >= nr) break;
+            float part = 0.0f;
+#pragma unroll
+            for (int h = 0; h < H; ++h) {
+              // weights of row j: four at a time when H is a multiple of 4
+              float wh;
+              if (H % 4 == 0) {
+                const float4 w4 = reinterpret_cast<const float4*>(w_s + j * H)[h / 4];
+                wh = (h & 3) == 0 ? w4.x : ((h & 3) == 1 ? w4.y : ((h & 3) == 2 ? w4.z : w4.w));
+              } else {
+                wh = w_s[j * H + h];
+              }
+              const uint32_t x = H < 16 ? v[q][rr * H + h] : v[q * kLdPerUnit + h / 16][h % 16];
+              const float xv = FP8 ? sgn * __uint_as_float(x) : __uint_as_float(x);
+              part = fmaf(wh, relu_nan(xv), part);
+            }
+            if (FP8) part *= mag;
+            if (c < oc) {
+              const float val = c < vis_s[j] ? part + 0.0f : -INFINITY;
+              if (p.stream_out) __stcs(ob + (int64_t)j * oc, val);
+              else ob[(int64_t)j * oc] = val;
+            }
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  } else if (FP8) {
+    // ------------------------------------------------------------ fp8 -> bf16 converter
+    // Thread (m, kh) widens the kh-th 64-element half of key row m.  The TMA
+    // stage holds 128-byte fp8 rows in the 128-byte swizzle (16-byte chunk j
+    // of row r at chunk j ^ (r % 8)); the bf16 operand rows use the same
+    // pattern, so both sides are bank-conflict free.
+    const int ct = threadIdx.x - 64 - kEpiThreads;  // 0..255
+    const int m = ct & (kBM - 1), kh = ct >> 7;
+    const int sw = m & 7;
+    int stage = 0, a = 0;
+    uint32_t phase = 0, aphase = 0;
+    bool ok = true;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      ok = wait_phase(&full[stage], phase, abort_flag, p.fault);
+      if (!ok) break;
+      ok = wait_phase(&aempty[a], aphase ^ 1u, abort_flag, p.fault);
+      if (!ok) break;
+      const uint8_t* src = S + stage * L.stage_bytes + m * 128;
+      uint4 in[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) in[i] = *reinterpret_cast<const uint4*>(src + (((4 * kh + i) ^ sw) << 4));
+      ptx::mbar_arrive(&empty[stage]);  // this thread's reads of the stage are done
+      uint8_t* dst = A + a * kTileBytes + kh * kHalfBytes + m * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint4 o0, o1;
+        o0.x = e4m3x2_to_bf16x2<0>(in[i].x);
+        o0.y = e4m3x2_to_bf16x2<1>(in[i].x);
+        o0.z = e4m3x2_to_bf16x2<0>(in[i].y);
+        o0.w = e4m3x2_to_bf16x2<1>(in[i].y);
+        o1.x = e4m3x2_to_bf16x2<0>(in[i].z);
+        o1.y = e4m3x2_to_bf16x2<1>(in[i].z);
+        o1.z = e4m3x2_to_bf16x2<0>(in[i].w);
+        o1.w = e4m3x2_to_bf16x2<1>(in[i].w);
+        *reinterpret_cast<uint4*>(dst + (((2 * i) ^ sw) << 4)) = o0;
+        *reinterpret_cast<uint4*>(dst + (((2 * i + 1) ^ sw) << 4)) = o1;
+      }
+      ptx::fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
+      ptx::mbar_arrive(&afull[a]);
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++a == kAStages) {
+        a = 0;
+        aphase ^= 1u;
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, (uint32_t)L.tmem_cols);
+}
+
+// Launch helpers, one translation unit per key type (umma_bf16.cu, umma_fp8.cu).
+cudaError_t launch_bf16(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                        const Layout& L, int grid, cudaStream_t s);
+cudaError_t launch_fp8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                       const Layout& L, int grid, cudaStream_t s);
+
+template <int H, bool FP8>
+cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up, const Layout& L,
+                     int grid, cudaStream_t s) {
+  auto kern = umma_score_kernel<H, FP8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, Roles<FP8>::kThreads, L.total, s>>>(kv, qm, up, L);
+  return cudaGetLastError();
+}
+
+template <bool FP8>
+cudaError_t launch_any(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                       const Layout& L, int grid, cudaStream_t s) {
+  switch (heads) {
+    case 1: return launch_h<1, FP8>(kv, qm, up, L, grid, s);
+    case 2: return launch_h<2, FP8>(kv, qm, up, L, grid, s);
+    case 4: return launch_h<4, FP8>(kv, qm, up, L, grid, s);
+    case 8: return launch_h<8, FP8>(kv, qm, up, L, grid, s);
+    case 16: return launch_h<16, FP8>(kv, qm, up, L, grid, s);
+    case 32: return launch_h<32, FP8>(kv, qm, up, L, grid, s);
+    default: return launch_h<64, FP8>(kv, qm, up, L, grid, s);
+  }
+}
+
+}  // namespace umma
+}  // namespace qsa

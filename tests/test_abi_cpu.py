@@ -129,6 +129,17 @@ def test_dispatch_decisions(lib):
     assert qsa.plan_variant(_desc(rows_per_req=1)) == qsa.VARIANT_ROWCORE
     # odd page size: only the CUDA-core scorer serves it
     assert qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256)) == qsa.VARIANT_ROWCORE
+    # MTP verify rows (4 rows x 4 heads = N 16) and fp8 keys -> tcgen05 scorer
+    assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA
+    d8 = _desc(rows_per_req=1, num_heads=64, page_cols=64, key_page_stride=64 * 132,
+               kv_dtype=qsa.KV_FP8_E4M3, scale_page_stride=64 * 132)
+    assert qsa.plan_variant(d8) == qsa.VARIANT_UMMA
+    # head counts the tcgen05 epilogue is not built for -> CUDA-core scorer
+    assert qsa.plan_variant(_desc(num_heads=3)) == qsa.VARIANT_ROWCORE
     qsa.force_variant(qsa.VARIANT_ROWCORE)
     assert qsa.plan_variant(_desc()) == qsa.VARIANT_ROWCORE
+    qsa.force_variant(qsa.VARIANT_UMMA)
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256))
+    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
     qsa.force_variant(qsa.VARIANT_AUTO)

@@ -301,3 +301,30 @@ def test_full_size_workload_sampled(oracle_mod, name):
 def test_no_kernel_gave_up_on_a_barrier():
     """Every bounded wait above completed: the device fault word is still clear."""
     assert qsa.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("variant", ["rowcore", "umma"])
+@pytest.mark.parametrize("sign", [1.0, -1.0])
+def test_fp8_every_finite_code_including_subnormals(oracle_mod, variant, sign):
+    """Column c holds code c in element 0 (all other elements zero); q = +-e0, w = 1,
+    scale = 2: the logit is relu(+-2 * e4m3(c)), exact in fp32 - so every code,
+    subnormals included, must decode exactly (no flush to zero)."""
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    n = len(codes)
+    spec = qi.custom("fp8_codes", 1, 1, 1, 16, [n], 256, k=8, kv_dtype=qi.KV_FP8, seed=3)
+    inp = qi.build_inputs(spec)
+    D, pc = 128, 16
+    inp.kv[:, : pc * D] = 0
+    inp.kv[:, pc * D:] = np.full((inp.num_pages, pc), 2.0, np.float32).view(np.uint8).reshape(inp.num_pages, -1)
+    for ci, code in enumerate(codes):
+        page = int(inp.block_table[0, ci // pc])
+        inp.kv[page, (ci % pc) * D] = code
+    q = np.zeros((1, 1, D), np.float32)
+    q[0, 0, 0] = sign
+    inp.q = qi._bf16_bits(q)
+    inp.weights = np.ones((1, 1), np.float32)
+    if not supported(inp, VARIANTS[variant]):
+        pytest.skip(f"{variant} does not serve this shape")
+    out, _, _ = gpu_logits(inp, VARIANTS[variant])
+    ref = oracle_mod.paged_mqa_logits(inp)
+    assert (out.cpu().numpy().view(np.uint32) == ref.view(np.uint32)).all()
