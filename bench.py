@@ -8,9 +8,12 @@ workload (two kernel launches).  Prints one JSON line.
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Timing: K steps back to back on one stream between a barrier and a device
-synchronize on both sides, CUDA events around each kernel; inputs and outputs
-rotate over enough copies that their footprint exceeds twice the L2, so no
-step reads another step's data from L2.  `value` is key-cache bytes processed
+synchronize on both sides, enqueued as CUDA graph replays (>= 16 steps a
+graph) so host launch overhead is not on the device timeline; CUDA events
+around the K steps give the step time, and graphs of scoring-only and
+top-k-only launches give each kernel's average launch time.  Inputs and
+outputs rotate over enough copies that their footprint exceeds twice the L2,
+so no step reads another step's data from L2.  `value` is key-cache bytes processed
 per second over the whole step (each request's visible keys counted once),
 summed over ranks with the max time over ranks.  Under torchrun each rank runs
 its own replica of the workload (weak scaling, no collective on the data path).
@@ -222,7 +225,10 @@ def oracle_sample_run(inp, requests, threads):
     return dt, key_bytes, len(rows)
 
 
-def cpu_baseline(inp, budget_s: float = 12.0):
+def cpu_baseline(inp, budget_s: float = 10.0):
+    """The oracle on the host cores: whole requests (scoring + top-k), repeated
+    until about budget_s seconds of work; prefill-sized requests are sampled by
+    rows instead.  Returns key-cache GB/s over the sample."""
     import oracle
 
     oracle.build()
@@ -230,15 +236,12 @@ def cpu_baseline(inp, budget_s: float = 12.0):
     spec = inp.spec
     rng = np.random.default_rng(0)
     order = rng.permutation(spec.num_requests).tolist()
-    dt1, _, _ = oracle_sample_run(inp, order[:1], threads)  # one request, to size the sample
-    n_req = max(1, min(spec.num_requests, int(budget_s / max(dt1, 1e-6) * 0.8)))
-    # a single request's rows may be many (prefill): cap rows instead
     if spec.rows_per_req > 64:
         t_rows = time.perf_counter()
         sub_rows = [order[0] * spec.rows_per_req + i for i in range(min(64, spec.rows_per_req))]
         oracle.paged_mqa_logits(inp, rows=sub_rows, threads=threads)
         per_row = (time.perf_counter() - t_rows) / len(sub_rows)
-        n_rows = max(1, min(spec.rows_per_req, int(budget_s / max(per_row, 1e-9) * 0.8)))
+        n_rows = max(1, min(spec.num_rows, int(budget_s / max(per_row, 1e-9) * 0.8)))
         rows = sorted(rng.choice(spec.num_rows, n_rows, replace=False).tolist())
         t0 = time.perf_counter()
         lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
@@ -249,11 +252,23 @@ def cpu_baseline(inp, budget_s: float = 12.0):
         key_bytes = spec.key_bytes_touched() * len(rows) / spec.num_rows
         sample = f"{len(rows)} of {spec.num_rows} rows (scoring + top-k), key bytes credited pro rata"
         return {"value": key_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                "sample": sample, "seconds": dt}
-    dt, kb, nrows = oracle_sample_run(inp, order[:n_req], threads)
-    return {"value": kb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n_req} of {spec.num_requests} requests ({nrows} rows, scoring + top-k)",
-            "seconds": dt}
+                "sample": sample, "seconds": round(dt, 3)}
+    dt1, _, _ = oracle_sample_run(inp, order[:1], threads)  # one request, to size the sample
+    per_pass = dt1 * spec.num_requests
+    if per_pass >= budget_s:
+        n_req = max(1, int(budget_s / max(dt1, 1e-9)))
+        dt, kb, nrows = oracle_sample_run(inp, order[:n_req], threads)
+        sample = f"{n_req} of {spec.num_requests} requests ({nrows} rows, scoring + top-k)"
+    else:
+        passes = max(1, int(budget_s / max(per_pass, 1e-9)))
+        dt = kb = 0
+        for _ in range(passes):
+            d, b, nrows = oracle_sample_run(inp, order, threads)
+            dt += d
+            kb += b
+        sample = f"the whole step (all {spec.num_requests} requests, {spec.num_rows} rows), {passes} times"
+    return {"value": kb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
+            "seconds": round(dt, 3)}
 
 
 def run_reference(args):
@@ -349,16 +364,17 @@ def run_gpu(args):
                f"single copy ({per_copy / 1e6:.0f} MB of inputs+outputs, larger than 2x L2)"
                if per_copy > 2 * l2 else f"single copy ({per_copy / 1e6:.0f} MB), L2 not defeated")
 
-    stream = torch.cuda.current_stream(dev)
-
     def score(d):
         torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
                                    page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
-                                   scale_offset=inp.scale_offset, out=d["out"], stream=stream)
+                                   scale_offset=inp.scale_offset, out=d["out"])
 
     def topk(d):
-        torch_api.select_topk(d["out"], d["visible"], k, out=d["idx"], stream=stream)
+        torch_api.select_topk(d["out"], d["visible"], k, out=d["idx"])
 
+    # eager warm-up (first calls set kernel attributes), then CUDA graphs: the
+    # host enqueues one graph per >= 16 steps, so launch overhead on the host
+    # never shows up in the device timings.
     for i in range(args.warmup):
         d = sets[i % copies]
         score(d)
@@ -366,34 +382,69 @@ def run_gpu(args):
     variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
     torch.cuda.synchronize(dev)
 
+    def capture(n_steps, do_score=True, do_topk=True):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                d = sets[i % copies]
+                if do_score:
+                    score(d)
+                if do_topk:
+                    topk(d)
+        return g
+
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    per_graph = copies * max(1, -(-16 // copies))
+    full_graphs, rem = divmod(K, per_graph)
+    g_step = capture(per_graph)
+    g_rem = capture(rem) if rem else None
+    for _ in range(max(1, -(-args.warmup // per_graph))):
+        g_step.replay()
+    torch.cuda.synchronize(dev)
+
+    stream = torch.cuda.current_stream(dev)
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
     time.sleep(0.3 if sampler else 0.0)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()
-    for i in range(K):
-        d = sets[i % copies]
-        ev[i][0].record(stream)
-        score(d)
-        ev[i][1].record(stream)
-        topk(d)
-        ev[i][2].record(stream)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(full_graphs):
+        g_step.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e_end.record(stream)
     torch.cuda.synchronize(dev)
     t1 = time.time()
     barrier()
     clocks = sampler.stop(t0, t1) if sampler else None
+    total_ms = e_start.elapsed_time(e_end)
 
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][2])
-    score_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    topk_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    # per-kernel launch times: graphs of scoring launches only / top-k only
+    def time_graph(g, n_launch, reps):
+        for _ in range(2):
+            g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return 1e3 * a.elapsed_time(b) / (reps * n_launch)
+
+    reps = max(1, min(full_graphs, 64))
+    g_score = capture(per_graph, do_topk=False)
+    g_topk = capture(per_graph, do_score=False)
+    score_us = time_graph(g_score, per_graph, reps)
+    topk_us = time_graph(g_topk, per_graph, reps)
+    del g_step, g_rem, g_score, g_topk
+
     max_ms = max_over_ranks(total_ms)
     ms_step = max_ms / K
     key_bytes = spec.key_bytes_touched()
     value = sum_over_ranks(key_bytes * K) / (max_ms / 1e3) / 1e9
-    score_us = 1e3 * sum(score_ms) / K
-    topk_us = 1e3 * sum(topk_ms) / K
 
     # roofline of the dominant kernel
     peaks = measured_peaks()
@@ -426,14 +477,14 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+        e0.record(torch.cuda.current_stream(dev))
         for _ in range(Ke):
             for name, t in host.items():
                 d[name].copy_(t, non_blocking=True)
             score(d)
             topk(d)
             out_host.copy_(d["idx"], non_blocking=True)
-        e1.record(stream)
+        e1.record(torch.cuda.current_stream(dev))
         torch.cuda.synchronize(dev)
         e_ms = max_over_ranks(e0.elapsed_time(e1))
         e2e = {"value": sum_over_ranks(key_bytes * Ke) / (e_ms / 1e3) / 1e9, "unit": "GB/s",

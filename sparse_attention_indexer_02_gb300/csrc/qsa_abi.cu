@@ -149,6 +149,12 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const fl
   int32_t variant = 0;
   st = qsa_plan_variant(d, &variant);
   if (st != QSA_OK) return st;
+  // the tcgen05 scorer bulk-copies fp8 scales, which needs a 16-byte aligned base
+  if (variant == QSA_VARIANT_UMMA && fp8 && !aligned(scales, 16)) {
+    if (g_forced_variant.load() == QSA_VARIANT_UMMA)
+      return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant needs 16-byte aligned fp8 scales");
+    variant = QSA_VARIANT_ROWCORE;
+  }
 
   qsa::ScoreParams p;
   p.q = static_cast<const uint16_t*>(q);

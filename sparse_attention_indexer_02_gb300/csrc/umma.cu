@@ -78,6 +78,10 @@ bool umma_supports(const qsa_paged_desc& d, const char** why) {
     *why = "page_cols must be a multiple of 8 that divides 128 or is a multiple of 128";
     return false;
   }
+  if (d.kv_dtype == QSA_KV_FP8_E4M3 && d.scale_page_stride % 16 != 0) {
+    *why = "fp8 scale_page_stride must be a multiple of 16 bytes for the bulk copies";
+    return false;
+  }
   if (d.out_cols > (int64_t)0x7FFFFF00LL) {
     *why = "out_cols too large for the tile index";
     return false;
@@ -117,6 +121,8 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   d.page_cols = p.page_cols;
   d.kv_dtype = p.fp8 ? QSA_KV_FP8_E4M3 : QSA_KV_BF16;
   d.out_cols = p.out_cols;
+  d.key_page_stride = p.key_page_stride;
+  d.scale_page_stride = p.scale_page_stride;
   if (!umma_supports(d, msg)) return cudaErrorInvalidValue;
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) {

@@ -44,6 +44,8 @@ constexpr int kHalfBytes = kBM * 128;       // one 64-element K-half of a bf16 k
 constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB
 constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
 constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
+constexpr int kFp8StageAlloc = kFp8StageBytes + 1024;  // + the block's 128 fp32 scales, 1024-aligned
+constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (see the converter)
 // Warp roles: 0 TMA, 1 MMA, then the epilogue warps (two per TMEM lane
 // quadrant for bf16 keys, one for fp8), then 8 fp8->bf16 converter warps
 // (fp8) or 4 spare warps that only take part in the CTA-wide barriers (bf16:
@@ -85,7 +87,7 @@ struct Layout {
   int32_t a_stages;     // fp8: bf16 operand stages written by the converter; bf16: 0
   int32_t tmem_cols;    // 2 accumulators of N columns, power of two >= 32
   uint32_t idesc;       // tcgen05 instruction descriptor for M = 128, this N
-  int32_t a_off, b_off, bar_off, misc_off, epi_off, sched_off, total;
+  int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, total;
 };
 
 inline Layout make_layout(int N, int groups, bool fp8) {
@@ -93,15 +95,18 @@ inline Layout make_layout(int N, int groups, bool fp8) {
   L.n = N;
   L.tmem_cols = 2 * N < 32 ? 32 : 2 * N;
   L.idesc = ptx::idesc_bf16_f32(kBM, N);
-  L.stage_bytes = fp8 ? kFp8StageBytes : kTileBytes;
+  L.stage_bytes = fp8 ? kFp8StageAlloc : kTileBytes;
   L.a_stages = fp8 ? kFp8ConvStages : 0;
-  const int tail = N * 256 + (2 * 8 + 2 * kFp8ConvStages + 7) * 8 + 32 + 2 * 256 * 4 + 8 * (groups + 1);
+  const int ring = fp8 ? kScaleRing * kBM * 4 : 0;
+  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 7) * 8 + 32 + 2 * 256 * 4 +
+                   8 * (groups + 1);
   int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;
   L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
   L.b_off = L.a_off + L.a_stages * kTileBytes;
-  L.bar_off = L.b_off + N * 256;
-  const int nbars = 2 * L.stages + 2 * L.a_stages + 2 + 2 + 3;
+  L.ring_off = L.b_off + N * 256;      // fp8 only: per-tile key scales
+  L.bar_off = L.ring_off + ring;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + (fp8 ? kScaleRing : 0) + 2 + 2 + 3;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4;        // pref[G + 1], gmax[G]
@@ -174,7 +179,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* afull = empty + kStages;          // fp8: converter -> MMA
   uint64_t* aempty = afull + kAStages;        // fp8: MMA -> converter
-  uint64_t* tfull = aempty + kAStages;
+  uint64_t* sfull = aempty + kAStages;        // fp8: converter -> epilogue, one per scale slot
+  uint64_t* tfull = sfull + (FP8 ? kScaleRing : 0);
+  float* scale_ring = reinterpret_cast<float*>(smem + L.ring_off);  // fp8: [kScaleRing][128]
   uint64_t* tempty = tfull + 2;
   uint64_t* qfull = tempty + 2;
   uint64_t* qempty = qfull + 1;
@@ -199,6 +206,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       ptx::mbar_init(&afull[s], R::kConvThreads);
       ptx::mbar_init(&aempty[s], 1);
     }
+    if (FP8)
+      for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], kBM);
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], kEpiThreads);
@@ -217,19 +226,29 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     ptx::prefetch_tmap(&kv_map);
     ptx::prefetch_tmap(&q_map);
   }
-  // Per-group tile counts from the visible counts (device data, no host sync).
-  for (int g = threadIdx.x; g < G; g += kThreads) {
-    const int b = g / p.groups_per_req, j = g % p.groups_per_req;
-    const int r0 = b * p.rows_per_req + j * p.group_rows;
-    const int nr = min(p.group_rows, p.rows_per_req - j * p.group_rows);
-    int64_t mv = 0;
-    for (int i = 0; i < nr; ++i) {
-      const int64_t v = clamp64(p.visible[r0 + i], 0, p.capacity);
-      mv = v > mv ? v : mv;
+  // Per-group widest visible count and tile count from the visible counts
+  // (device data, no host sync): every thread takes rows, four loads in flight.
+  for (int g = threadIdx.x; g < G; g += kThreads) gmax[g] = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < p.num_rows; r0 += 4 * kThreads) {
+    int32_t v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * kThreads + threadIdx.x;
+      v[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
     }
-    gmax[g] = (int32_t)mv;
-    pref[g] = (int32_t)((mv + kBM - 1) / kBM);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int r = r0 + u * kThreads + threadIdx.x;
+      const int32_t vc = (int32_t)clamp64(v[u], 0, p.capacity);
+      if (r < p.num_rows && vc > 0) {
+        const int b = r / p.rows_per_req;
+        atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
+      }
+    }
   }
+  __syncthreads();
+  for (int g = threadIdx.x; g < G; g += kThreads) pref[g] = (gmax[g] + kBM - 1) / kBM;
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -266,19 +285,21 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     const int tiles_per_batch = 32 / bpt;       // one box per lane per batch
     const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // per K-half (bf16) or per page (fp8)
     const uint32_t copies = FP8 ? 1u : 2u;
-    // Page id of this lane's box in the batch starting at tile tb (-1: none).
+    // Page id of this lane's box in the batch starting at tile tb (kNoPage: none).
     // Lane l covers tile tb + l / bpt, box l % bpt.
+    constexpr int32_t kNoPage = INT32_MIN;
     auto lane_page = [&](int tb) -> int32_t {
       const int tl = tb + lane / bpt, box = lane % bpt;
-      if (tl >= t_end) return -1;
+      if (tl >= t_end) return kNoPage;
       const int gl = find_group(pref, G, tl);
       const int c0 = (tl - pref[gl]) * kBM;
       const int lim = gmax[gl] - c0;
       const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
-      if (box >= nbox) return -1;
+      if (box >= nbox) return kNoPage;
       const int64_t lp = (int64_t)c0 / pc + (pc >= kBM ? 0 : box);
-      const int32_t v = __ldg(p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp);
-      return v < 0 ? 0 : (v >= p.num_pages ? p.num_pages - 1 : v);
+      // raw table entry: clamped where it is used, so this load stays in
+      // flight while the current batch is issued
+      return __ldg(p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp);
     };
     int stage = 0;
     uint32_t phase = 0;
@@ -287,7 +308,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     uint32_t q_loads = 0;
     uint32_t filled_mask = 0, last_phase_bits = 0;
     bool ok = true;
-    int32_t cur = t_begin < t_end ? lane_page(t_begin) : -1;
+    int32_t cur = t_begin < t_end ? lane_page(t_begin) : kNoPage;
     for (int tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
       // the next batch's block-table entries load while this batch is issued
       const int32_t nxt = lane_page(tb + tiles_per_batch);
@@ -312,14 +333,21 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         }
         ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, p.fault);
         if (!ok) break;
-        if (lane == 0) ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes);
+        if (lane == 0)
+          ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
         __syncwarp();
-        if (lane / bpt == i && cur >= 0) {
+        if (lane / bpt == i && cur != kNoPage) {
+          cur = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);
           const int box = lane % bpt;
           const int y = pc >= kBM ? c0 % pc : 0;
           uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * 128u;
           ptx::tma_load_3d(dst, &kv_map, 0, y, cur, &full[stage], policy);
           if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, cur, &full[stage], policy);
+          if (FP8)  // the box's scales land after the key rows of the stage (plain bulk copy:
+                    // 16-byte aligned source, destination and size)
+            ptx::bulk_load(S + stage * L.stage_bytes + kFp8StageBytes + box * p.box_rows * 4,
+                           p.scales + (int64_t)cur * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
+                           &full[stage], policy);
         }
         filled_mask |= 1u << stage;
         last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
@@ -401,52 +429,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     const int m = quad * 32 + lane;            // key row of the tile = TMEM lane
     const int64_t oc = p.out_cols;
 
-    // (1) this CTA's share of the -inf tail.  Group g's tail is its tiles
-    // [T_g, tiles_cap), i.e. columns [T_g * 128, out_cols) of its rows; the
-    // CTA takes a contiguous slice of the tail tiles of all groups and writes
-    // each group's part of it as a plain row-by-row range (16-byte streaming
-    // stores when rows are 16-byte aligned).
-    {
-      const int64_t Tc = p.tiles_cap;
-      const int64_t F = (int64_t)G * Tc - total;
-      int64_t f = F * blockIdx.x / gridDim.x;
-      const int64_t f1 = F * (blockIdx.x + 1) / gridDim.x;
-      if (f < f1) {
-        // fill prefix fp(g) = g * Tc - pref[g] is non-decreasing; find the group of f
-        int lo = 0, hi = G;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if ((int64_t)mid * Tc - pref[mid] <= f) lo = mid;
-          else hi = mid;
-        }
-        const bool vec = (oc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
-        const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int g = lo; f < f1 && g < G; ++g) {
-          const int64_t fpg = (int64_t)g * Tc - pref[g];
-          const int Tg = pref[g + 1] - pref[g];
-          const int64_t fe = min(f1, fpg + (Tc - Tg));
-          if (f >= fe) continue;
-          const int64_t ca = (Tg + (f - fpg)) * kBM;
-          const int64_t cb = min((Tg + (fe - fpg)) * kBM, oc);
-          f = fe;
-          if (ca >= cb) continue;
-          const int jj = g % p.groups_per_req;
-          const int64_t r0 = (int64_t)(g / p.groups_per_req) * p.rows_per_req + jj * p.group_rows;
-          const int nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
-          for (int j = 0; j < nr; ++j) {
-            float* o = p.out + (r0 + j) * oc;
-            if (vec) {
-              for (int64_t cc = ca + 4 * et; cc < cb; cc += 4 * kEpiThreads)
-                __stcs(reinterpret_cast<float4*>(o + cc), ninf4);
-            } else {
-              for (int64_t cc = ca + et; cc < cb; cc += kEpiThreads) __stcs(o + cc, -INFINITY);
-            }
-          }
-        }
-      }
-    }
-
-    // (2) computed tiles.  Column n of the accumulator is (row n / H, head
+    // (1) computed tiles.  Column n of the accumulator is (row n / H, head
     // n % H).  A "unit" is the smallest run of 16-column TMEM loads that holds
     // whole rows: one load (16 / H rows) for H <= 16, H / 16 loads (one row)
     // for H > 16.  The warps of a quadrant take alternate units.
@@ -477,13 +460,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       // per row after the head sum.
       float sgn = 1.0f, mag = 1.0f;
       if (FP8) {
-        float sc = 0.0f;
-        if (c < gmax[g]) {
-          const int32_t v = __ldg(p.block_table + (int64_t)b * p.max_pages + c / p.page_cols);
-          const int32_t pg = v < 0 ? 0 : (v >= p.num_pages ? p.num_pages - 1 : v);
-          sc = __ldg(reinterpret_cast<const float*>(p.scales + (int64_t)pg * p.scale_stride +
-                                                    4 * (c % p.page_cols)));
-        }
+        const int i = t - t_begin;
+        ok = wait_phase(&sfull[i % kScaleRing], (uint32_t)(i / kScaleRing) & 1u, abort_flag, p.fault);
+        if (!ok) break;
+        const float sc = scale_ring[(i % kScaleRing) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
@@ -541,6 +521,52 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+
+    // (2) this CTA's share of the -inf tail, after its tiles (the pipeline
+    // starts at once).  Group g's tail is its tiles
+    // [T_g, tiles_cap), i.e. columns [T_g * 128, out_cols) of its rows; the
+    // CTA takes a contiguous slice of the tail tiles of all groups and writes
+    // each group's part of it as a plain row-by-row range (16-byte streaming
+    // stores when rows are 16-byte aligned).
+    if (ok) {
+      const int64_t Tc = p.tiles_cap;
+      const int64_t F = (int64_t)G * Tc - total;
+      int64_t f = F * blockIdx.x / gridDim.x;
+      const int64_t f1 = F * (blockIdx.x + 1) / gridDim.x;
+      if (f < f1) {
+        // fill prefix fp(g) = g * Tc - pref[g] is non-decreasing; find the group of f
+        int lo = 0, hi = G;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if ((int64_t)mid * Tc - pref[mid] <= f) lo = mid;
+          else hi = mid;
+        }
+        const bool vec = (oc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+        const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        for (int g = lo; f < f1 && g < G; ++g) {
+          const int64_t fpg = (int64_t)g * Tc - pref[g];
+          const int Tg = pref[g + 1] - pref[g];
+          const int64_t fe = min(f1, fpg + (Tc - Tg));
+          if (f >= fe) continue;
+          const int64_t ca = (Tg + (f - fpg)) * kBM;
+          const int64_t cb = min((Tg + (fe - fpg)) * kBM, oc);
+          f = fe;
+          if (ca >= cb) continue;
+          const int jj = g % p.groups_per_req;
+          const int64_t r0 = (int64_t)(g / p.groups_per_req) * p.rows_per_req + jj * p.group_rows;
+          const int nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+          for (int j = 0; j < nr; ++j) {
+            float* o = p.out + (r0 + j) * oc;
+            if (vec) {
+              for (int64_t cc = ca + 4 * et; cc < cb; cc += 4 * kEpiThreads)
+                __stcs(reinterpret_cast<float4*>(o + cc), ninf4);
+            } else {
+              for (int64_t cc = ca + et; cc < cb; cc += kEpiThreads) __stcs(o + cc, -INFINITY);
+            }
+          }
+        }
+      }
+    }
   } else if (FP8) {
     // ------------------------------------------------------------ fp8 -> bf16 converter
     // Thread (m, kh) widens the kh-th 64-element half of key row m.  The TMA
@@ -562,6 +588,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       uint4 in[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) in[i] = *reinterpret_cast<const uint4*>(src + (((4 * kh + i) ^ sw) << 4));
+      if (kh == 0) {
+        // Tile i's scales go to ring slot i % kScaleRing.  The slot is free:
+        // this converter may be at tile i only after the MMA of tile
+        // i - kScaleRing + kFp8ConvStages finished, which needed the epilogue
+        // to release the accumulator of tile i - kScaleRing (same parity), and
+        // the epilogue reads a tile's scales before releasing it.
+        const int i = t - t_begin;
+        scale_ring[(i % kScaleRing) * kBM + m] =
+            *reinterpret_cast<const float*>(S + stage * L.stage_bytes + kFp8StageBytes + m * 4);
+        ptx::mbar_arrive(&sfull[i % kScaleRing]);
+      }
       ptx::mbar_arrive(&empty[stage]);  // this thread's reads of the stage are done
       uint8_t* dst = A + a * kTileBytes + kh * kHalfBytes + m * 128;
 #pragma unroll
