@@ -254,18 +254,17 @@ def cpu_baseline(inp, budget_s: float = 10.0):
         return {"value": key_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
                 "sample": sample, "seconds": round(dt, 3)}
     dt1, _, _ = oracle_sample_run(inp, order[:1], threads)  # one request, to size the sample
-    per_pass = dt1 * spec.num_requests
-    if per_pass >= budget_s:
-        n_req = max(1, int(budget_s / max(dt1, 1e-9)))
+    if dt1 * spec.num_requests / threads >= budget_s:
+        n_req = max(1, min(spec.num_requests, int(budget_s * threads / max(dt1, 1e-9))))
         dt, kb, nrows = oracle_sample_run(inp, order[:n_req], threads)
         sample = f"{n_req} of {spec.num_requests} requests ({nrows} rows, scoring + top-k)"
     else:
-        passes = max(1, int(budget_s / max(per_pass, 1e-9)))
-        dt = kb = 0
-        for _ in range(passes):
+        passes = dt = kb = 0
+        while dt < budget_s:  # whole steps until the budget is spent
             d, b, nrows = oracle_sample_run(inp, order, threads)
             dt += d
             kb += b
+            passes += 1
         sample = f"the whole step (all {spec.num_requests} requests, {spec.num_rows} rows), {passes} times"
     return {"value": kb / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": sample,
             "seconds": round(dt, 3)}
