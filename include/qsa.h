@@ -142,10 +142,13 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
 /*
  * qsa_plan_variant - host-only dispatch decision for `desc` (no CUDA call).
  * Writes the qsa_variant qsa_paged_mqa_logits would launch (honouring
- * qsa_force_variant) to *variant.  Single-row bf16 decode with few heads goes
- * to the CUDA-core scorer (vLLM #62589 "Dispatch": one-row kernel for
- * single-row decode, decided from host metadata, no device sync); shapes the
- * tcgen05 scorer supports go to it; everything else to the CUDA-core scorer.
+ * qsa_force_variant) to *variant.  The choice uses host metadata only, with no
+ * device sync, as vLLM #62589 "Dispatch" does for its one-row kernel.  On
+ * GB300 the tcgen05 scorer measures faster than the CUDA-core one-row scorer
+ * at every row count (single-row decode included), so shapes it supports go
+ * to it; everything else (head counts other than 1, 2, 4, ..., 64, page sizes
+ * that are not a multiple of 8 dividing 128 or a multiple of 128, misaligned
+ * fp8 scales) goes to the CUDA-core scorer.
  */
 qsa_status qsa_plan_variant(const qsa_paged_desc* desc, int32_t* variant);
 

@@ -114,10 +114,11 @@ qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) {
     if (!qsa::umma_supports(*d, &why))
       return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant cannot serve this shape: %s", why);
     *variant = QSA_VARIANT_UMMA;
-  } else if (d->rows_per_req == 1 && d->kv_dtype == QSA_KV_BF16 && d->num_heads <= 8) {
-    // single-row bf16 decode with few heads: the CUDA-core one-row scorer
-    *variant = QSA_VARIANT_ROWCORE;
   } else if (qsa::umma_supports(*d, &why)) {
+    // Measured on GB300: the tcgen05 scorer is faster than the CUDA-core
+    // one-row scorer at every row count, single-row decode included (its
+    // padded N = 16 costs nothing against HBM), so it takes every shape it
+    // serves; the one-row scorer serves the rest.
     *variant = QSA_VARIANT_UMMA;
   } else {
     *variant = QSA_VARIANT_ROWCORE;

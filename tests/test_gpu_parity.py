@@ -241,6 +241,30 @@ def test_topk_rows_longer_than_the_shared_memory_cache(oracle_mod):
     assert_topk_strict(idx, oracle_mod.select_topk(x, np.array(vis, np.int32), 2048))
 
 
+@pytest.mark.parametrize("rows", [3, 40, 100, 200])
+def test_topk_cluster_sizes_and_single_cta_path(oracle_mod, rows):
+    """Few rows split over clusters of 8, 4 or 2 CTAs; many rows use one CTA a row."""
+    rng = np.random.default_rng(rows)
+    vis = rng.integers(2000, 9000, size=rows).astype(np.int32)
+    vis[0] = 9000
+    x = qi.random_logit_rows(rng, rows, 9003, vis, zero_frac=0.1)
+    xt = torch.from_numpy(x).cuda()
+    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 1000)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 1000))
+
+
+def test_topk_many_long_rows_read_from_global_memory(oracle_mod):
+    """More rows than the cluster path takes, each longer than the shared-memory cache."""
+    rows = 160
+    rng = np.random.default_rng(77)
+    vis = np.full(rows, 50000, np.int32)
+    vis[::7] = 49153
+    x = qi.random_logit_rows(rng, rows, 50004, vis, zero_frac=0.05)
+    xt = torch.from_numpy(x).cuda()
+    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 2048)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 2048))
+
+
 def test_topk_threshold_ties_take_the_lowest_columns(oracle_mod):
     # 3000 exact zeros around the k-th place: the lowest-column zeros must win
     x = np.zeros((2, 5000), np.float32)
