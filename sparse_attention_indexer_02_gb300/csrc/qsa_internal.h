@@ -30,8 +30,11 @@ struct ScoreParams {
 cudaError_t launch_rowcore(const ScoreParams& p, cudaStream_t stream, const char** msg);
 bool umma_supports(const qsa_paged_desc& d, const char** why);
 cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg);
-// Reads (and optionally clears) the device fault word the scoring kernels set
-// when a bounded wait gives up.  Synchronises the device.
+// Device address of the fault word on the current device (bit 0: a scoring
+// kernel's bounded wait gave up; bit 1: a top-k kernel's).
+cudaError_t fault_word_address(unsigned int** out);
+// Reads (and optionally clears) the device fault word the kernels set when a
+// bounded wait gives up.  Synchronises the device.
 cudaError_t read_fault_word(uint32_t* flags, bool clear);
 cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride,
                         const int32_t* visible, int32_t k, int32_t* out, cudaStream_t stream);

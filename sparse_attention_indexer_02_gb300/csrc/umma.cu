@@ -18,25 +18,6 @@ __device__ unsigned int g_fault_word = 0;
 
 namespace {
 
-// Device address of g_fault_word on the current device (looked up once per device).
-cudaError_t fault_word_address(unsigned int** out) {
-  static std::mutex mu;
-  static unsigned int* addr[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < 64 && addr[dev]) {
-    *out = addr[dev];
-    return cudaSuccess;
-  }
-  void* a = nullptr;
-  e = cudaGetSymbolAddress(&a, g_fault_word);
-  if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64) addr[dev] = static_cast<unsigned int*>(a);
-  *out = static_cast<unsigned int*>(a);
-  return cudaSuccess;
-}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -69,6 +50,26 @@ void group_shape(const qsa_paged_desc& d, int* G_rows, int* N) {
 
 }  // namespace
 }  // namespace umma
+
+// Device address of g_fault_word on the current device (looked up once per device).
+cudaError_t fault_word_address(unsigned int** out) {
+  static std::mutex mu;
+  static unsigned int* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < 64 && addr[dev]) {
+    *out = addr[dev];
+    return cudaSuccess;
+  }
+  void* a = nullptr;
+  e = cudaGetSymbolAddress(&a, umma::g_fault_word);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64) addr[dev] = static_cast<unsigned int*>(a);
+  *out = static_cast<unsigned int*>(a);
+  return cudaSuccess;
+}
 
 using namespace umma;
 

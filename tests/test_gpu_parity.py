@@ -243,14 +243,29 @@ def test_topk_rows_longer_than_the_shared_memory_cache(oracle_mod):
 
 @pytest.mark.parametrize("rows", [3, 40, 100, 200])
 def test_topk_cluster_sizes_and_single_cta_path(oracle_mod, rows):
-    """Few rows split over clusters of 8, 4 or 2 CTAs; many rows use one CTA a row."""
+    """Few long rows split over clusters of 8, 4 or 2 CTAs (rows of at most 12288
+    visible columns inside such a launch are done by one CTA of their cluster);
+    many rows use one CTA a row."""
     rng = np.random.default_rng(rows)
-    vis = rng.integers(2000, 9000, size=rows).astype(np.int32)
-    vis[0] = 9000
-    x = qi.random_logit_rows(rng, rows, 9003, vis, zero_frac=0.1)
+    vis = rng.integers(2000, 40000, size=rows).astype(np.int32)
+    vis[:3] = [40000, 12288, 12289]
+    x = qi.random_logit_rows(rng, rows, 40003, vis, zero_frac=0.1)
     xt = torch.from_numpy(x).cuda()
-    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 1000)
-    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 1000))
+    for k in (1000, 2048):
+        idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), k)
+        assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+
+
+@pytest.mark.parametrize("rows", [1, 3, 40])
+def test_topk_short_rows_one_cta(oracle_mod, rows):
+    """Rows no longer than 12288 columns take the one-CTA kernel at any row count."""
+    rng = np.random.default_rng(rows + 11)
+    vis = rng.integers(2049, 12288, size=rows).astype(np.int32)
+    vis[0] = 12288
+    x = qi.random_logit_rows(rng, rows, 12288, vis, zero_frac=0.1)
+    xt = torch.from_numpy(x).cuda()
+    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 2048)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 2048))
 
 
 def test_topk_many_long_rows_read_from_global_memory(oracle_mod):
