@@ -165,10 +165,11 @@ const char* qsa_status_string(int32_t status);
 const char* qsa_last_error(void);
 
 /*
- * qsa_device_status - the library's device fault word.  Non-zero (bit 0) after
- * a scoring kernel gave up waiting on one of its internal barriers (about one
+ * qsa_device_status - the library's device fault word.  Bit 0 is set after a
+ * scoring kernel gave up waiting on one of its internal barriers (about one
  * second): that launch left its output incomplete and returned early instead
- * of hanging the GPU.  Synchronises the current device, then writes the word
+ * of hanging the GPU.  Bit 1: a top-k launch gave up waiting for its row copy
+ * (its selection for that row is unspecified).  Synchronises the current device, then writes the word
  * to *flags (host pointer) and clears it when `clear` is non-zero.
  */
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear);

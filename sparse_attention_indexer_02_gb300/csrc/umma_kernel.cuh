@@ -59,6 +59,7 @@ struct Roles {
   static constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 };
 constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr int kFastSchedRows = 256;              // up to this many rows one warp builds the schedule
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in limit per CTA
 
 
@@ -98,7 +99,7 @@ inline Layout make_layout(int N, int groups, bool fp8) {
   L.stage_bytes = fp8 ? kFp8StageAlloc : kTileBytes;
   L.a_stages = fp8 ? kFp8ConvStages : 0;
   const int ring = fp8 ? kScaleRing * kBM * 4 : 0;
-  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 7) * 8 + 32 + 2 * 256 * 4 +
+  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 +
                    8 * (groups + 1);
   int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;
@@ -106,7 +107,7 @@ inline Layout make_layout(int N, int groups, bool fp8) {
   L.b_off = L.a_off + L.a_stages * kTileBytes;
   L.ring_off = L.b_off + N * 256;      // fp8 only: per-tile key scales
   L.bar_off = L.ring_off + ring;
-  const int nbars = 2 * L.stages + 2 * L.a_stages + (fp8 ? kScaleRing : 0) + 2 + 2 + 3;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + (fp8 ? kScaleRing : 0) + 2 + 2 + 4;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4;        // pref[G + 1], gmax[G]
@@ -141,6 +142,28 @@ __device__ __forceinline__ int find_group(const int32_t* pref, int num_groups, i
   return lo;
 }
 
+// Exclusive scan (one warp) of the per-group tile counts in pref[0..G), total
+// in pref[G].
+__device__ __forceinline__ void scan_tiles(int32_t* pref, int G, int lane) {
+  const int per = (G + 31) / 32;
+  const int lo = min(G, lane * per), hi = min(G, lo + per);
+  int s = 0;
+  for (int i = lo; i < hi; ++i) s += pref[i];
+  int incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int run = incl - s;
+  for (int i = lo; i < hi; ++i) {
+    const int t = pref[i];
+    pref[i] = run;
+    run += t;
+  }
+  if (lane == 31) pref[G] = incl;
+}
+
 __device__ __forceinline__ void epi_bar(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
@@ -158,6 +181,50 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
   uint32_t r;
   asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));  // 2^120 in both halves
   return r;
+}
+
+// The -inf tail: group g's columns [T_g * 128, out_cols) for its rows, where
+// T_g is its scheduled tile count.  The CTA takes a contiguous slice of all
+// groups' tail tiles (flattened group-major) and writes each group's part as
+// plain row ranges, 16-byte streaming stores when rows are 16-byte aligned.
+template <int kNT>
+__device__ __forceinline__ void fill_tail(const UmmaParams& p, const int32_t* pref, int G, int total, int tid) {
+  const int64_t oc = p.out_cols;
+  const int64_t Tc = p.tiles_cap;
+  const int64_t F = (int64_t)G * Tc - total;
+  int64_t f = F * blockIdx.x / gridDim.x;
+  const int64_t f1 = F * (blockIdx.x + 1) / gridDim.x;
+  if (f >= f1) return;
+  // fill prefix fp(g) = g * Tc - pref[g] is non-decreasing; find the group of f
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)mid * Tc - pref[mid] <= f) lo = mid;
+    else hi = mid;
+  }
+  const bool vec = (oc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+  const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  for (int g = lo; f < f1 && g < G; ++g) {
+    const int64_t fpg = (int64_t)g * Tc - pref[g];
+    const int Tg = pref[g + 1] - pref[g];
+    const int64_t fe = min(f1, fpg + (Tc - Tg));
+    if (f >= fe) continue;
+    const int64_t ca = (Tg + (f - fpg)) * kBM;
+    const int64_t cb = min((Tg + (fe - fpg)) * kBM, oc);
+    f = fe;
+    if (ca >= cb) continue;
+    const int jj = g % p.groups_per_req;
+    const int64_t r0 = (int64_t)(g / p.groups_per_req) * p.rows_per_req + jj * p.group_rows;
+    const int nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+    for (int j = 0; j < nr; ++j) {
+      float* o = p.out + (r0 + j) * oc;
+      if (vec) {
+        for (int64_t cc = ca + 4 * tid; cc < cb; cc += 4 * kNT) __stcs(reinterpret_cast<float4*>(o + cc), ninf4);
+      } else {
+        for (int64_t cc = ca + tid; cc < cb; cc += kNT) __stcs(o + cc, -INFINITY);
+      }
+    }
+  }
 }
 
 template <int H, bool FP8>
@@ -197,6 +264,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.num_groups;
 
+  uint64_t* setup = mma_done + 1;  // one-warp schedule and TMEM allocation done
+  // Few rows: warp 0 alone builds the schedule from visible counts it loads
+  // first thing, and starts producing at once; the other warps wait on
+  // `setup`.  Many rows: every thread takes part, with CTA barriers.
+  const bool fast = p.num_rows <= kFastSchedRows;
+  int32_t vfast[kFastSchedRows / 32];
+  if (fast && warp == 0) {
+#pragma unroll
+    for (int u = 0; u < kFastSchedRows / 32; ++u) {
+      const int r = u * 32 + lane;
+      vfast[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
+    }
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -215,65 +295,82 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     ptx::mbar_init(qfull, 1);
     ptx::mbar_init(qempty, 1);
     ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(setup, 2);
     *abort_flag = 0;
     ptx::fence_mbar_init();
-  }
-  if (warp == 1) {
-    ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
-    ptx::tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&kv_map);
     ptx::prefetch_tmap(&q_map);
   }
-  // Per-group widest visible count and tile count from the visible counts
-  // (device data, no host sync): every thread takes rows, four loads in flight.
-  for (int g = threadIdx.x; g < G; g += kThreads) gmax[g] = 0;
-  __syncthreads();
-  for (int r0 = 0; r0 < p.num_rows; r0 += 4 * kThreads) {
-    int32_t v[4];
+  if (!fast && warp == 1) {
+    ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
+    ptx::tmem_relinquish();
+  }
+  if (!fast)
+    for (int g = threadIdx.x; g < G; g += kThreads) gmax[g] = 0;
+  __syncthreads();  // barriers initialised
+  uint32_t tmem_base = 0;
+  bool setup_ok = true;
+  if (fast) {
+    if (warp == 0) {
+      for (int g = lane; g < G; g += 32) gmax[g] = 0;
+      __syncwarp();
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = r0 + u * kThreads + threadIdx.x;
-      v[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
+      for (int u = 0; u < kFastSchedRows / 32; ++u) {
+        const int r = u * 32 + lane;
+        const int32_t vc = (int32_t)clamp64(vfast[u], 0, p.capacity);
+        if (r < p.num_rows && vc > 0) {
+          const int b = r / p.rows_per_req;
+          atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
+        }
+      }
+      __syncwarp();
+      for (int g = lane; g < G; g += 32) pref[g] = (gmax[g] + kBM - 1) / kBM;
+      __syncwarp();
+      scan_tiles(pref, G, lane);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(setup);
+    } else {
+      if (warp == 1) {
+        ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
+        ptx::tmem_relinquish();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(setup);
+      }
+      setup_ok = wait_phase(setup, 0, abort_flag, p.fault);
+      ptx::tc_fence_after();
+      tmem_base = *tmem_slot;
     }
+  } else {
+    // Per-group widest visible count and tile count from the visible counts
+    // (device data, no host sync): every thread takes rows, four loads in flight.
+    for (int r0 = 0; r0 < p.num_rows; r0 += 4 * kThreads) {
+      int32_t v[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = r0 + u * kThreads + threadIdx.x;
-      const int32_t vc = (int32_t)clamp64(v[u], 0, p.capacity);
-      if (r < p.num_rows && vc > 0) {
-        const int b = r / p.rows_per_req;
-        atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
+      for (int u = 0; u < 4; ++u) {
+        const int r = r0 + u * kThreads + threadIdx.x;
+        v[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r0 + u * kThreads + threadIdx.x;
+        const int32_t vc = (int32_t)clamp64(v[u], 0, p.capacity);
+        if (r < p.num_rows && vc > 0) {
+          const int b = r / p.rows_per_req;
+          atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
+        }
       }
     }
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += kThreads) pref[g] = (gmax[g] + kBM - 1) / kBM;
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    tmem_base = *tmem_slot;
+    if (warp == 0) scan_tiles(pref, G, lane);
+    __syncthreads();
   }
-  __syncthreads();
-  for (int g = threadIdx.x; g < G; g += kThreads) pref[g] = (gmax[g] + kBM - 1) / kBM;
-  ptx::tc_fence_before();
-  __syncthreads();
-  ptx::tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  if (warp == 0) {  // exclusive scan of the tile counts, total in pref[G]
-    const int per = (G + 31) / 32;
-    const int lo = min(G, lane * per), hi = min(G, lo + per);
-    int s = 0;
-    for (int i = lo; i < hi; ++i) s += pref[i];
-    int incl = s;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - s;
-    for (int i = lo; i < hi; ++i) {
-      const int t = pref[i];
-      pref[i] = run;
-      run += t;
-    }
-    if (lane == 31) pref[G] = incl;
-  }
-  __syncthreads();
-  const int total = pref[G];
+  const int total = setup_ok ? pref[G] : 0;
   const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
 
@@ -522,51 +619,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       }
     }
 
-    // (2) this CTA's share of the -inf tail, after its tiles (the pipeline
-    // starts at once).  Group g's tail is its tiles
-    // [T_g, tiles_cap), i.e. columns [T_g * 128, out_cols) of its rows; the
-    // CTA takes a contiguous slice of the tail tiles of all groups and writes
-    // each group's part of it as a plain row-by-row range (16-byte streaming
-    // stores when rows are 16-byte aligned).
-    if (ok) {
-      const int64_t Tc = p.tiles_cap;
-      const int64_t F = (int64_t)G * Tc - total;
-      int64_t f = F * blockIdx.x / gridDim.x;
-      const int64_t f1 = F * (blockIdx.x + 1) / gridDim.x;
-      if (f < f1) {
-        // fill prefix fp(g) = g * Tc - pref[g] is non-decreasing; find the group of f
-        int lo = 0, hi = G;
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if ((int64_t)mid * Tc - pref[mid] <= f) lo = mid;
-          else hi = mid;
-        }
-        const bool vec = (oc & 3) == 0 && (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
-        const float4 ninf4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        for (int g = lo; f < f1 && g < G; ++g) {
-          const int64_t fpg = (int64_t)g * Tc - pref[g];
-          const int Tg = pref[g + 1] - pref[g];
-          const int64_t fe = min(f1, fpg + (Tc - Tg));
-          if (f >= fe) continue;
-          const int64_t ca = (Tg + (f - fpg)) * kBM;
-          const int64_t cb = min((Tg + (fe - fpg)) * kBM, oc);
-          f = fe;
-          if (ca >= cb) continue;
-          const int jj = g % p.groups_per_req;
-          const int64_t r0 = (int64_t)(g / p.groups_per_req) * p.rows_per_req + jj * p.group_rows;
-          const int nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
-          for (int j = 0; j < nr; ++j) {
-            float* o = p.out + (r0 + j) * oc;
-            if (vec) {
-              for (int64_t cc = ca + 4 * et; cc < cb; cc += 4 * kEpiThreads)
-                __stcs(reinterpret_cast<float4*>(o + cc), ninf4);
-            } else {
-              for (int64_t cc = ca + et; cc < cb; cc += kEpiThreads) __stcs(o + cc, -INFINITY);
-            }
-          }
-        }
-      }
-    }
+    // (2) fp8: this CTA's share of the -inf tail, after its tiles (the
+    // converter warps are busy until then).  bf16: the spare warps write it.
+    if (FP8 && ok && setup_ok) fill_tail<kEpiThreads>(p, pref, G, total, et);
   } else if (FP8) {
     // ------------------------------------------------------------ fp8 -> bf16 converter
     // Thread (m, kh) widens the kh-th 64-element half of key row m.  The TMA
@@ -628,6 +683,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     }
   }
 
+  if (!FP8 && warp >= 2 + R::kEpiWarps && setup_ok) {
+    // ------------------------------------------------------------ bf16 spare warps
+    // the -inf tail, while the pipeline starts up and streams keys
+    fill_tail<R::kConvThreads>(p, pref, G, total, (int)threadIdx.x - 64 - kEpiThreads);
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();

@@ -91,6 +91,9 @@ SMALL = [
     ("rows64_prefill_like", 1, 80, 4, 64, [200 + i // 4 for i in range(80)], 256, 64),
     ("visible_full_and_empty", 3, 2, 4, 16, [96, 96, 0, 0, 95, 1], 96, 8),
     ("page128_single", 2, 2, 4, 128, [700, 701, 129, 128], 768, 100),
+    # more than 256 rows: the schedule is built by the whole CTA
+    ("rows300_one_request", 1, 300, 4, 64, [100 + i // 3 for i in range(300)], 256, 32),
+    ("rows260_single_row_requests", 260, 1, 4, 16, [0, 17, 130, 255, 256], 288, 16),
 ]
 
 
