@@ -271,11 +271,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   const bool fast = p.num_rows <= kFastSchedRows;
   int32_t vfast[kFastSchedRows / 32];
   if (fast && warp == 0) {
+    // in-range address in every lane; rows past num_rows are masked at use, so
+    // nothing waits for these loads before the barriers are initialised
 #pragma unroll
-    for (int u = 0; u < kFastSchedRows / 32; ++u) {
-      const int r = u * 32 + lane;
-      vfast[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
-    }
+    for (int u = 0; u < kFastSchedRows / 32; ++u) vfast[u] = __ldg(p.visible + min(u * 32 + lane, p.num_rows - 1));
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -382,22 +381,24 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     const int tiles_per_batch = 32 / bpt;       // one box per lane per batch
     const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // per K-half (bf16) or per page (fp8)
     const uint32_t copies = FP8 ? 1u : 2u;
-    // Page id of this lane's box in the batch starting at tile tb (kNoPage: none).
-    // Lane l covers tile tb + l / bpt, box l % bpt.
-    constexpr int32_t kNoPage = INT32_MIN;
-    auto lane_page = [&](int tb) -> int32_t {
+    // Block-table entry of this lane's box in the batch starting at tile tb
+    // (null: no box).  Lane l covers tile tb + l / bpt, box l % bpt.
+    auto lane_entry = [&](int tb) -> const int32_t* {
       const int tl = tb + lane / bpt, box = lane % bpt;
-      if (tl >= t_end) return kNoPage;
+      if (tl >= t_end) return nullptr;
       const int gl = find_group(pref, G, tl);
       const int c0 = (tl - pref[gl]) * kBM;
       const int lim = gmax[gl] - c0;
       const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
-      if (box >= nbox) return kNoPage;
+      if (box >= nbox) return nullptr;
       const int64_t lp = (int64_t)c0 / pc + (pc >= kBM ? 0 : box);
-      // raw table entry: clamped where it is used, so this load stays in
-      // flight while the current batch is issued
-      return __ldg(p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp);
+      return p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp;
     };
+    // Every lane loads from a valid address (the table's first entry when it
+    // has no box) and nothing reads the value until its copy is issued, so
+    // the load stays in flight while the current batch is issued.  (A select
+    // on the loaded value would wait for it right here.)
+    auto load_entry = [&](const int32_t* e) -> int32_t { return __ldg(e != nullptr ? e : p.block_table); };
     int stage = 0;
     uint32_t phase = 0;
     int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
@@ -405,10 +406,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     uint32_t q_loads = 0;
     uint32_t filled_mask = 0, last_phase_bits = 0;
     bool ok = true;
-    int32_t cur = t_begin < t_end ? lane_page(t_begin) : kNoPage;
+    const int32_t* cur_e = t_begin < t_end ? lane_entry(t_begin) : nullptr;
+    int32_t cur = load_entry(cur_e);
     for (int tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
       // the next batch's block-table entries load while this batch is issued
-      const int32_t nxt = lane_page(tb + tiles_per_batch);
+      const int32_t* nxt_e = lane_entry(tb + tiles_per_batch);
+      const int32_t nxt = load_entry(nxt_e);
       for (int i = 0; i < tiles_per_batch && tb + i < t_end; ++i) {
         const int t = tb + i;
         while (t >= pref[g + 1]) ++g;
@@ -433,17 +436,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         if (lane == 0)
           ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
         __syncwarp();
-        if (lane / bpt == i && cur != kNoPage) {
-          cur = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);
+        if (lane / bpt == i && cur_e != nullptr) {
+          const int32_t pg = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);  // clamp: no fault
           const int box = lane % bpt;
           const int y = pc >= kBM ? c0 % pc : 0;
           uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * 128u;
-          ptx::tma_load_3d(dst, &kv_map, 0, y, cur, &full[stage], policy);
-          if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, cur, &full[stage], policy);
+          ptx::tma_load_3d(dst, &kv_map, 0, y, pg, &full[stage], policy);
+          if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, pg, &full[stage], policy);
           if (FP8)  // the box's scales land after the key rows of the stage (plain bulk copy:
                     // 16-byte aligned source, destination and size)
             ptx::bulk_load(S + stage * L.stage_bytes + kFp8StageBytes + box * p.box_rows * 4,
-                           p.scales + (int64_t)cur * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
+                           p.scales + (int64_t)pg * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
                            &full[stage], policy);
         }
         filled_mask |= 1u << stage;
@@ -454,6 +457,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         }
       }
       cur = nxt;
+      cur_e = nxt_e;
     }
     // Drain: every copy this warp issued has landed before the CTA tears down.
     if (lane == 0 && *abort_flag) {
