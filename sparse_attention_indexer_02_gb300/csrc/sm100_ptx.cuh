@@ -42,6 +42,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// ---- programmatic dependent launch -------------------------------------------
+
+// Waits until the grid this launch depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) has completed
+// and its memory operations are visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream begin launching (its CTAs run their
+// prologue and then wait in grid_dep_wait for this grid to complete).
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- TMA --------------------------------------------------------------------
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

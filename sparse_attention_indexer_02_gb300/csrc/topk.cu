@@ -197,6 +197,8 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const RowArgs a) {
   extern __shared__ uint4 dyn_row[];
   float* cache = reinterpret_cast<float*>(dyn_row);
   __shared__ RowShared sh;
+  ptx::grid_dep_wait();  // the logits come from the previous kernel in the stream
+  ptx::grid_dep_launch();
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int64_t row = blockIdx.x;
   const int k = a.k;
@@ -702,7 +704,18 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   e = cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  topk_row_kernel<<<(unsigned)num_rows, kRT, smem, stream>>>(ra);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_rows, 1, 1);
+  cfg.blockDim = dim3(kRT, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dep_wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_row_kernel, ra);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

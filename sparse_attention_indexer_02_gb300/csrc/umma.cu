@@ -156,6 +156,11 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   up.num_groups = p.num_requests * up.groups_per_req;
   up.tiles_cap = (int32_t)((p.out_cols + kBM - 1) / kBM);
   up.box_rows = p.page_cols < kBM ? p.page_cols : kBM;
+  up.bpt_shift = 0;
+  while (p.page_cols < kBM && (p.page_cols << up.bpt_shift) < kBM) ++up.bpt_shift;
+  up.pc_shift = -1;
+  for (int sh = 0; sh < 31; ++sh)
+    if ((1 << sh) == p.page_cols) up.pc_shift = sh;
   up.stream_out = (int64_t)p.num_rows * p.out_cols * 4 > (64LL << 20) ? 1 : 0;
   up.keep_keys = up.groups_per_req > 1 ? 1 : 0;
 

@@ -75,6 +75,8 @@ struct UmmaParams {
   int64_t capacity;
   int32_t num_rows, rows_per_req, num_heads, page_cols, max_pages, num_pages;
   int32_t group_rows, groups_per_req, num_groups, tiles_cap, box_rows;
+  int32_t bpt_shift;  // log2(pages per 128-column tile) when page_cols < 128, else 0
+  int32_t pc_shift;   // log2(page_cols) when page_cols is a power of two, else -1
   int32_t stream_out;  // logits far larger than L2: write them with evict-first stores
   int32_t keep_keys;   // several row groups reuse each key tile: keep keys in L2
 };
@@ -269,13 +271,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   // first thing, and starts producing at once; the other warps wait on
   // `setup`.  Many rows: every thread takes part, with CTA barriers.
   const bool fast = p.num_rows <= kFastSchedRows;
-  int32_t vfast[kFastSchedRows / 32];
-  if (fast && warp == 0) {
-    // in-range address in every lane; rows past num_rows are masked at use, so
-    // nothing waits for these loads before the barriers are initialised
-#pragma unroll
-    for (int u = 0; u < kFastSchedRows / 32; ++u) vfast[u] = __ldg(p.visible + min(u * 32 + lane, p.num_rows - 1));
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
@@ -299,6 +294,17 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&kv_map);
     ptx::prefetch_tmap(&q_map);
+  }
+  // Everything above overlaps the previous kernel in the stream; no global
+  // memory is touched before it has completed.
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
+  int32_t vfast[kFastSchedRows / 32];
+  if (fast && warp == 0) {
+    // in-range address in every lane; rows past num_rows are masked at use, so
+    // nothing waits for these loads until they are used
+#pragma unroll
+    for (int u = 0; u < kFastSchedRows / 32; ++u) vfast[u] = __ldg(p.visible + min(u * 32 + lane, p.num_rows - 1));
   }
   if (!fast && warp == 1) {
     ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
@@ -327,7 +333,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       __syncwarp();
       scan_tiles(pref, G, lane);
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(setup);
+      // warp 0 arrives on `setup` once its first copies are issued (below):
+      // until then the other warps stay parked and leave it the issue slots
     } else {
       if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
@@ -377,22 +384,27 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     const uint64_t policy = p.keep_keys ? ptx::policy_evict_last() : ptx::policy_evict_first();
     const int pc = p.page_cols;
-    const int bpt = pc >= kBM ? 1 : kBM / pc;  // boxes (pages) per full tile, <= 16
-    const int tiles_per_batch = 32 / bpt;       // one box per lane per batch
+    const int bsh = p.bpt_shift;
+    const int bpt = 1 << bsh;                   // boxes (pages) per full tile, <= 16
+    const int tiles_per_batch = 32 >> bsh;      // one box per lane per batch
+    // page index and slot of column c (a power-of-two page size below 128
+    // columns always; otherwise a 32-bit division)
+    auto page_of = [&](int c) { return p.pc_shift >= 0 ? c >> p.pc_shift : c / pc; };
+    auto req_of = [&](int g) { return p.groups_per_req == 1 ? g : g / p.groups_per_req; };
     const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // per K-half (bf16) or per page (fp8)
     const uint32_t copies = FP8 ? 1u : 2u;
     // Block-table entry of this lane's box in the batch starting at tile tb
     // (null: no box).  Lane l covers tile tb + l / bpt, box l % bpt.
     auto lane_entry = [&](int tb) -> const int32_t* {
-      const int tl = tb + lane / bpt, box = lane % bpt;
+      const int tl = tb + (lane >> bsh), box = lane & (bpt - 1);
       if (tl >= t_end) return nullptr;
       const int gl = find_group(pref, G, tl);
       const int c0 = (tl - pref[gl]) * kBM;
       const int lim = gmax[gl] - c0;
-      const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
+      const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) >> p.pc_shift);
       if (box >= nbox) return nullptr;
-      const int64_t lp = (int64_t)c0 / pc + (pc >= kBM ? 0 : box);
-      return p.block_table + (int64_t)(gl / p.groups_per_req) * p.max_pages + lp;
+      const int lp = page_of(c0) + box;
+      return p.block_table + (int64_t)req_of(gl) * p.max_pages + lp;
     };
     // Every lane loads from a valid address (the table's first entry when it
     // has no box) and nothing reads the value until its copy is issued, so
@@ -406,6 +418,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     uint32_t q_loads = 0;
     uint32_t filled_mask = 0, last_phase_bits = 0;
     bool ok = true;
+    bool released = !fast;  // fast schedule: `setup` not yet arrived on by this warp
     const int32_t* cur_e = t_begin < t_end ? lane_entry(t_begin) : nullptr;
     int32_t cur = load_entry(cur_e);
     for (int tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
@@ -415,11 +428,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       for (int i = 0; i < tiles_per_batch && tb + i < t_end; ++i) {
         const int t = tb + i;
         while (t >= pref[g + 1]) ++g;
-        const int b = g / p.groups_per_req, jj = g % p.groups_per_req;
+        const int b = req_of(g), jj = g - b * p.groups_per_req;
         const int r0 = b * p.rows_per_req + jj * p.group_rows;
         const int c0 = (t - pref[g]) * kBM;
         const int lim = gmax[g] - c0;  // visible columns in this tile (>= 1)
-        const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) / pc);
+        const int nbox = pc >= kBM ? 1 : min(bpt, (lim + pc - 1) >> p.pc_shift);
         if (g != qg) {
           if (q_loads > 0) ok = wait_phase(qempty, (q_loads - 1) & 1, abort_flag, p.fault);
           if (!ok) break;
@@ -436,10 +449,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         if (lane == 0)
           ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
         __syncwarp();
-        if (lane / bpt == i && cur_e != nullptr) {
+        if ((lane >> bsh) == i && cur_e != nullptr) {
           const int32_t pg = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);  // clamp: no fault
-          const int box = lane % bpt;
-          const int y = pc >= kBM ? c0 % pc : 0;
+          const int box = lane & (bpt - 1);
+          const int y = pc >= kBM ? c0 - page_of(c0) * pc : 0;
           uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * 128u;
           ptx::tma_load_3d(dst, &kv_map, 0, y, pg, &full[stage], policy);
           if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, pg, &full[stage], policy);
@@ -448,6 +461,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
             ptx::bulk_load(S + stage * L.stage_bytes + kFp8StageBytes + box * p.box_rows * 4,
                            p.scales + (int64_t)pg * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
                            &full[stage], policy);
+        }
+        if (!released) {
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(setup);
+          released = true;
         }
         filled_mask |= 1u << stage;
         last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
@@ -459,6 +477,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       cur = nxt;
       cur_e = nxt_e;
     }
+    if (!released && lane == 0) ptx::mbar_arrive(setup);  // no tile, or gave up before the first
     // Drain: every copy this warp issued has landed before the CTA tears down.
     if (lane == 0 && *abort_flag) {
       for (int s = 0; s < kStages; ++s)
@@ -710,7 +729,20 @@ cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaPar
   auto kern = umma_score_kernel<H, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
-  kern<<<grid, Roles<FP8>::kThreads, L.total, s>>>(kv, qm, up, L);
+  // programmatic stream serialisation: the launch may begin while the
+  // previous kernel finishes; the kernel waits for it before touching memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(Roles<FP8>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)L.total;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, kv, qm, up, L);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
