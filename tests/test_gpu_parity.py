@@ -246,9 +246,9 @@ def test_topk_rows_longer_than_the_shared_memory_cache(oracle_mod):
 
 @pytest.mark.parametrize("rows", [3, 40, 100, 200])
 def test_topk_cluster_sizes_and_single_cta_path(oracle_mod, rows):
-    """Few long rows split over clusters of 8, 4 or 2 CTAs (rows of at most 12288
-    visible columns inside such a launch are done by one CTA of their cluster);
-    many rows use one CTA a row."""
+    """Few rows are split over clusters of 8 or 2 CTAs (3 and 40 rows), many
+    rows use one CTA a row (100 and 200); rows of 4003..40000 columns, the
+    stride not a multiple of 4 (plain loads fill the cache)."""
     rng = np.random.default_rng(rows)
     vis = rng.integers(2000, 40000, size=rows).astype(np.int32)
     vis[:3] = [40000, 12288, 12289]
@@ -260,8 +260,9 @@ def test_topk_cluster_sizes_and_single_cta_path(oracle_mod, rows):
 
 
 @pytest.mark.parametrize("rows", [1, 3, 40])
-def test_topk_short_rows_one_cta(oracle_mod, rows):
-    """Rows no longer than 12288 columns take the one-CTA kernel at any row count."""
+def test_topk_short_rows(oracle_mod, rows):
+    """Rows of at most 12288 columns with a 16-byte aligned stride (bulk copies
+    fill the cache), over clusters of 8 (1 and 3 rows) and 2 CTAs (40 rows)."""
     rng = np.random.default_rng(rows + 11)
     vis = rng.integers(2049, 12288, size=rows).astype(np.int32)
     vis[0] = 12288
@@ -281,6 +282,21 @@ def test_topk_many_long_rows_read_from_global_memory(oracle_mod):
     xt = torch.from_numpy(x).cuda()
     idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 2048)
     assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 2048))
+
+
+@pytest.mark.parametrize("rows,n", [(200, 30000), (2, 65536)])
+def test_topk_candidate_list_overflow(oracle_mod, rows, n):
+    """Rows whose first-digit bin holds more keys than a CTA's candidate list
+    (all values equal): the CTAs fall back to scanning their whole segment; the
+    lowest columns win the tie (one CTA a row for 200 rows, clusters of 8 for 2)."""
+    x = np.full((rows, n + 4), 1.5, np.float32)
+    x[:, n:] = 9.0  # past the visible count: never selected
+    x[1, 100] = 2.0  # one larger value in row 1
+    vis = np.full(rows, n, np.int32)
+    xt = torch.from_numpy(x).cuda()
+    idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), 2048)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 2048))
+    assert idx[0].tolist() == list(range(2048))
 
 
 def test_topk_threshold_ties_take_the_lowest_columns(oracle_mod):
