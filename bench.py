@@ -109,7 +109,7 @@ def algorithmic_bytes(spec: qi.Spec):
         "visible": R * 4,
         "logits_out": R * spec.out_cols * 4,
     }
-    vis = spec.visible.astype(np.int64)
+    vis = spec.live_visible().astype(np.int64)
     topk = {"logits_in": int(np.minimum(vis, spec.out_cols).sum()) * 4, "visible": R * 4,
             "indices_out": R * spec.k * 4}
     return score, topk
@@ -218,7 +218,7 @@ def oracle_sample_run(inp, requests, threads):
     rows = [r for b in requests for r in range(b * spec.rows_per_req, (b + 1) * spec.rows_per_req)]
     t0 = time.perf_counter()
     lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
-    oracle.select_topk(lg, spec.visible[rows], spec.k, threads=threads)
+    oracle.select_topk(lg, spec.live_visible()[rows], spec.k, threads=threads)
     dt = time.perf_counter() - t0
     vis = spec.visible.reshape(spec.num_requests, spec.rows_per_req).max(axis=1)
     key_bytes = int(sum(int(vis[b]) for b in requests)) * spec.key_bytes_per_col
@@ -245,7 +245,7 @@ def cpu_baseline(inp, budget_s: float = 10.0):
         rows = sorted(rng.choice(spec.num_rows, n_rows, replace=False).tolist())
         t0 = time.perf_counter()
         lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
-        oracle.select_topk(lg, spec.visible[rows], spec.k, threads=threads)
+        oracle.select_topk(lg, spec.live_visible()[rows], spec.k, threads=threads)
         dt = time.perf_counter() - t0
         # keys of a request are shared by its rows: credit each sampled row with
         # its share of the request's key bytes
@@ -366,10 +366,10 @@ def run_gpu(args):
     def score(d):
         torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
                                    page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
-                                   scale_offset=inp.scale_offset, out=d["out"])
+                                   scale_offset=inp.scale_offset, out=d["out"], next_n_lens=d.get("next_n_lens"))
 
-    def topk(d):
-        torch_api.select_topk(d["out"], d["visible"], k, out=d["idx"])
+    def topk(d):  # ragged call: the top-k reads the live rows' visible counts
+        torch_api.select_topk(d["out"], d.get("visible_live", d["visible"]), k, out=d["idx"])
 
     # eager warm-up (first calls set kernel attributes), then CUDA graphs: the
     # host enqueues one graph per >= 16 steps, so launch overhead on the host

@@ -120,6 +120,25 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* desc, const void* q, const
                                 float* out_logits, void* stream);
 
 /*
+ * qsa_paged_mqa_logits_ragged - qsa_paged_mqa_logits with a live-row count per
+ * request (aiter #4221 "Ragged next_n for confidence-scheduled verification":
+ * a request's leading next_n_lens[b] rows are live, the rest stay -inf).
+ *
+ * Row i of request b (r = b*rows_per_req + i) is live when
+ * i < clamp(next_n_lens[b], 0, rows_per_req); a live row is scored exactly as
+ * qsa_paged_mqa_logits scores it, and every logit of a dead row is -inf,
+ * whatever its q, weights and visible count (its keys are not read).
+ *
+ *   next_n_lens  int32 [num_requests] (device), 4-byte aligned, or NULL: every
+ *                row live (the call is then qsa_paged_mqa_logits).
+ * Other arguments, errors and ownership as qsa_paged_mqa_logits.
+ */
+qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* desc, const void* q, const float* weights,
+                                       const void* kv_cache, const float* scales,
+                                       const int32_t* block_table, const int32_t* visible_cols,
+                                       const int32_t* next_n_lens, float* out_logits, void* stream);
+
+/*
  * qsa_select_topk - per-row top-k column indices of a logits matrix.
  *
  * For each row r (vLLM #62589 "Details": top-k reads only [0, visible)):

@@ -84,10 +84,14 @@ def e4m3_value(code: int) -> float:
 
 
 def paged_mqa_logits(inp, rows: Optional[Sequence[int]] = None, threads: Optional[int] = None,
-                     *, q=None, weights=None, kv=None, block_table=None, visible=None) -> np.ndarray:
+                     *, q=None, weights=None, kv=None, block_table=None, visible=None,
+                     next_n_lens="spec") -> np.ndarray:
     """Oracle logits for ``inp`` (a ``qsa_inputs.Inputs``) as float32 [len(rows) or R, out_cols].
 
-    Keyword overrides replace single tensors (for invariance tests)."""
+    Keyword overrides replace single tensors (for invariance tests).  With live-row
+    counts (``next_n_lens``, default: the spec's), aiter #4221 "Ragged next_n":
+    request b's leading min(next_n_lens[b], rows_per_req) rows are scored and every
+    column of its other rows is -inf, i.e. those rows see no column."""
     lib = _load()
     s = inp.spec
     q = np.ascontiguousarray(inp.q if q is None else q, dtype=np.uint16)
@@ -95,6 +99,11 @@ def paged_mqa_logits(inp, rows: Optional[Sequence[int]] = None, threads: Optiona
     kvb = np.ascontiguousarray(inp.kv if kv is None else kv, dtype=np.uint8)
     bt = np.ascontiguousarray(inp.block_table if block_table is None else block_table, dtype=np.int32)
     vis = np.ascontiguousarray(s.visible if visible is None else visible, dtype=np.int32)
+    nn = s.next_n_lens if isinstance(next_n_lens, str) else next_n_lens
+    if nn is not None:
+        live_n = np.clip(np.asarray(nn, dtype=np.int64), 0, s.rows_per_req)
+        live = (np.arange(s.rows_per_req)[None, :] < live_n[:, None]).reshape(-1)
+        vis = np.ascontiguousarray(np.where(live, vis, 0), dtype=np.int32)
     sel = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     n = s.num_rows if sel is None else len(sel)
     out = np.empty((n, s.out_cols), dtype=np.float32)

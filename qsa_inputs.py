@@ -75,12 +75,27 @@ class Spec:
     seed: int
     head_dim: int = HEAD_DIM
     max_pages: Optional[int] = None  # block-table row width; default covers out_cols
+    next_n_lens: Optional[np.ndarray] = None  # int32 [B] live rows per request (ragged call), or None
 
     def __post_init__(self):
         self.visible = np.ascontiguousarray(self.visible, dtype=np.int32)
         assert self.visible.shape == (self.num_rows,)
+        if self.next_n_lens is not None:
+            self.next_n_lens = np.ascontiguousarray(self.next_n_lens, dtype=np.int32)
+            assert self.next_n_lens.shape == (self.num_requests,)
         if self.max_pages is None:
             self.max_pages = max(1, -(-self.out_cols // self.page_cols))
+
+    def live_rows(self) -> np.ndarray:
+        """bool [R]: row i of request b is live when i < next_n_lens[b] (all rows without it)."""
+        if self.next_n_lens is None:
+            return np.ones(self.num_rows, dtype=bool)
+        nn = np.clip(self.next_n_lens.astype(np.int64), 0, self.rows_per_req)
+        return (np.arange(self.rows_per_req)[None, :] < nn[:, None]).reshape(-1)
+
+    def live_visible(self) -> np.ndarray:
+        """Visible counts with dead rows at 0 (the columns whose keys are read)."""
+        return np.where(self.live_rows(), self.visible, 0).astype(np.int32)
 
     @property
     def num_rows(self) -> int:
@@ -91,13 +106,13 @@ class Spec:
         return self.head_dim * 2 if self.kv_dtype == KV_BF16 else self.head_dim + 4
 
     def pages_needed(self) -> np.ndarray:
-        """Per request: pages that hold at least one visible column."""
-        vis = self.visible.reshape(self.num_requests, self.rows_per_req).max(axis=1)
+        """Per request: pages that hold at least one visible column of a live row."""
+        vis = self.live_visible().reshape(self.num_requests, self.rows_per_req).max(axis=1)
         return -(-vis.astype(np.int64) // self.page_cols)
 
     def key_bytes_touched(self) -> int:
-        """Algorithmic key-cache bytes: each request's visible columns, once."""
-        vis = self.visible.reshape(self.num_requests, self.rows_per_req).max(axis=1)
+        """Algorithmic key-cache bytes: each request's visible columns (live rows), once."""
+        vis = self.live_visible().reshape(self.num_requests, self.rows_per_req).max(axis=1)
         return int(vis.astype(np.int64).sum()) * self.key_bytes_per_col
 
 
@@ -242,6 +257,17 @@ def prefill_chunk() -> Spec:
                 BASE_SEED + 4)
 
 
+def ragged_nn8() -> Spec:
+    """aiter #4221 ragged mix: 116 requests x next_n 8, next_n_lens ~ U{1..8}, fp8
+    block-flat KV block 64, 32 heads, prompts ~ U[32K, 128K] tokens, k 2048."""
+    rng = np.random.default_rng(BASE_SEED + 5)
+    L = rng.integers(32768, 131072 + 1, size=116)
+    nn = rng.integers(1, 8 + 1, size=116).astype(np.int32)
+    vis = decode_visible(L.tolist(), 8)
+    return Spec("ragged_116x8_nn1-8_fp8_h32", 116, 8, 32, 64, 32832, 2048, KV_FP8, vis, BASE_SEED + 5,
+                next_n_lens=nn)
+
+
 WORKLOADS = {
     "tiny_mtp": tiny_mtp,
     "single_row_decode": single_row_decode,
@@ -251,15 +277,18 @@ WORKLOADS = {
     "mtp3_large_p64": lambda: mtp3_large(64),
     "fp8_h64": fp8_h64,
     "prefill_chunk": prefill_chunk,
+    "ragged_nn8": ragged_nn8,
 }
 
 
 def custom(name: str, num_requests: int, rows_per_req: int, num_heads: int, page_cols: int,
            visible: Sequence[int], out_cols: int, k: int = 64, kv_dtype: int = KV_BF16,
-           seed: int = 7, max_pages: Optional[int] = None) -> Spec:
+           seed: int = 7, max_pages: Optional[int] = None,
+           next_n_lens: Optional[Sequence[int]] = None) -> Spec:
     """Small ad-hoc shapes for tests."""
+    nn = None if next_n_lens is None else np.asarray(next_n_lens, dtype=np.int32)
     return Spec(name, num_requests, rows_per_req, num_heads, page_cols, out_cols, k, kv_dtype,
-                np.asarray(visible, dtype=np.int32), seed, max_pages=max_pages)
+                np.asarray(visible, dtype=np.int32), seed, max_pages=max_pages, next_n_lens=nn)
 
 
 def random_logit_rows(rng: np.random.Generator, num_rows: int, width: int,
@@ -309,4 +338,7 @@ def device_tensors(inp: Inputs, device="cuda", pin: bool = False) -> dict:
         "block_table": t(inp.block_table),
         "visible": t(inp.spec.visible),
     }
+    if inp.spec.next_n_lens is not None:  # ragged call: live rows per request, and the
+        d["next_n_lens"] = t(inp.spec.next_n_lens)  # visible counts a top-k of it reads
+        d["visible_live"] = t(inp.spec.live_visible())
     return d

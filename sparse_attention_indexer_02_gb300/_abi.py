@@ -20,7 +20,7 @@ VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA = -1, 0, 1
 VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma"}
 
 # Every symbol include/qsa.h declares.
-EXPORTED = ("qsa_paged_mqa_logits", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
@@ -58,6 +58,8 @@ def load_library():
         vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
         lib.qsa_paged_mqa_logits.restype = ctypes.c_int
         lib.qsa_paged_mqa_logits.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_paged_mqa_logits_ragged.restype = ctypes.c_int
+        lib.qsa_paged_mqa_logits_ragged.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_select_topk.restype = ctypes.c_int
         lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         lib.qsa_plan_variant.restype = ctypes.c_int
@@ -117,10 +119,16 @@ def make_desc(num_requests, rows_per_req, num_heads, page_cols, max_pages, num_p
 
 
 def paged_mqa_logits(desc: PagedDesc, q, weights, kv_cache, scales, block_table, visible_cols,
-                     out_logits, stream=None) -> None:
-    st = load_library().qsa_paged_mqa_logits(ctypes.byref(desc), _addr(q), _addr(weights), _addr(kv_cache),
+                     out_logits, stream=None, next_n_lens=None) -> None:
+    lib = load_library()
+    if next_n_lens is None:
+        st = lib.qsa_paged_mqa_logits(ctypes.byref(desc), _addr(q), _addr(weights), _addr(kv_cache),
+                                      _addr(scales), _addr(block_table), _addr(visible_cols),
+                                      _addr(out_logits), _stream(stream))
+    else:
+        st = lib.qsa_paged_mqa_logits_ragged(ctypes.byref(desc), _addr(q), _addr(weights), _addr(kv_cache),
                                              _addr(scales), _addr(block_table), _addr(visible_cols),
-                                             _addr(out_logits), _stream(stream))
+                                             _addr(next_n_lens), _addr(out_logits), _stream(stream))
     _check(st)
 
 

@@ -33,6 +33,19 @@ __device__ __forceinline__ int64_t clamp64(int64_t v, int64_t lo, int64_t hi) {
   return v < lo ? lo : (v > hi ? hi : v);
 }
 
+// Visible count of row r with the live-row rule of the ragged call: row i of
+// request b sees no column when i >= next_n_lens[b] (clamped to the rows of a
+// request); next_n_lens null means every row is live.
+__device__ __forceinline__ int64_t row_visible(const int32_t* visible, const int32_t* next_n_lens, int64_t r,
+                                               int rows_per_req, int64_t capacity) {
+  int64_t v = clamp64(visible[r], 0, capacity);
+  if (next_n_lens != nullptr) {
+    const int64_t b = r / rows_per_req;
+    if (r - b * rows_per_req >= clamp64(next_n_lens[b], 0, rows_per_req)) v = 0;
+  }
+  return v;
+}
+
 // 16-byte read-only global load that bypasses L1 allocation (streamed keys).
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 r;

@@ -130,6 +130,14 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const fl
                                 const void* kv_cache, const float* scales,
                                 const int32_t* block_table, const int32_t* visible_cols,
                                 float* out_logits, void* stream) {
+  return qsa_paged_mqa_logits_ragged(d, q, weights, kv_cache, scales, block_table, visible_cols, nullptr,
+                                     out_logits, stream);
+}
+
+qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* d, const void* q, const float* weights,
+                                       const void* kv_cache, const float* scales,
+                                       const int32_t* block_table, const int32_t* visible_cols,
+                                       const int32_t* next_n_lens, float* out_logits, void* stream) {
   qsa_status st = validate_desc(d);
   if (st != QSA_OK) return st;
   const int64_t rows = (int64_t)d->num_requests * d->rows_per_req;
@@ -145,8 +153,9 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const fl
   if (!aligned(q, 16) || !aligned(kv_cache, 16))
     return fail(QSA_ERR_INVALID_ARG, "q and kv_cache must be 16-byte aligned");
   if (!aligned(weights, 4) || !aligned(block_table, 4) || !aligned(visible_cols, 4) ||
-      !aligned(out_logits, 4) || (fp8 && !aligned(scales, 4)))
-    return fail(QSA_ERR_INVALID_ARG, "weights, block_table, visible_cols, out_logits, scales must be 4-byte aligned");
+      !aligned(out_logits, 4) || (fp8 && !aligned(scales, 4)) || !aligned(next_n_lens, 4))
+    return fail(QSA_ERR_INVALID_ARG,
+                "weights, block_table, visible_cols, next_n_lens, out_logits, scales must be 4-byte aligned");
   int32_t variant = 0;
   st = qsa_plan_variant(d, &variant);
   if (st != QSA_OK) return st;
@@ -164,6 +173,7 @@ qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const fl
   p.scales = reinterpret_cast<const uint8_t*>(scales);
   p.block_table = block_table;
   p.visible = visible_cols;
+  p.next_n_lens = next_n_lens;
   p.out = out_logits;
   p.out_cols = d->out_cols;
   p.key_page_stride = d->key_page_stride;

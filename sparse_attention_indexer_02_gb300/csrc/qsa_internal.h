@@ -16,6 +16,7 @@ struct ScoreParams {
   const uint8_t* scales;    // fp8 scales base (NULL for bf16)
   const int32_t* block_table;
   const int32_t* visible;
+  const int32_t* next_n_lens;  // [num_requests] live rows of each request, or null (all live)
   float* out;
   int64_t out_cols;
   int64_t key_page_stride;

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, HR >= 8 ? 1 : 2) rowcore_kernel(cons
   const int64_t chunk = bid / p.num_rows;
   const int64_t c0 = chunk * kChunk;
   const int64_t c_end = c0 + kChunk < p.out_cols ? c0 + kChunk : p.out_cols;
-  const int64_t vis = clamp64(p.visible[row], 0, p.capacity);
+  const int64_t vis = row_visible(p.visible, p.next_n_lens, row, p.rows_per_req, p.capacity);
   float* out_row = p.out + row * p.out_cols;
 
   if (c0 >= vis) {  // column chunk past the visible range: mask only, no key traffic

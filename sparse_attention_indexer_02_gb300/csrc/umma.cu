@@ -142,6 +142,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   up.weights = p.weights;
   up.block_table = p.block_table;
   up.visible = p.visible;
+  up.next_n_lens = p.next_n_lens;
   up.out = p.out;
   up.out_cols = p.out_cols;
   up.capacity = p.capacity;

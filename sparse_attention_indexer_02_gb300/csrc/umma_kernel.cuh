@@ -70,6 +70,7 @@ struct UmmaParams {
   const float* weights;
   const int32_t* block_table;
   const int32_t* visible;
+  const int32_t* next_n_lens;  // live rows per request, or null (all live)
   float* out;
   int64_t out_cols;
   int64_t capacity;
@@ -299,12 +300,16 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   // memory is touched before it has completed.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
-  int32_t vfast[kFastSchedRows / 32];
+  int32_t vfast[kFastSchedRows / 32], nfast[kFastSchedRows / 32];
   if (fast && warp == 0) {
     // in-range address in every lane; rows past num_rows are masked at use, so
     // nothing waits for these loads until they are used
 #pragma unroll
-    for (int u = 0; u < kFastSchedRows / 32; ++u) vfast[u] = __ldg(p.visible + min(u * 32 + lane, p.num_rows - 1));
+    for (int u = 0; u < kFastSchedRows / 32; ++u) {
+      const int r = min(u * 32 + lane, p.num_rows - 1);
+      vfast[u] = __ldg(p.visible + r);
+      nfast[u] = p.next_n_lens != nullptr ? __ldg(p.next_n_lens + r / p.rows_per_req) : p.rows_per_req;
+    }
   }
   if (!fast && warp == 1) {
     ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
@@ -322,11 +327,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 #pragma unroll
       for (int u = 0; u < kFastSchedRows / 32; ++u) {
         const int r = u * 32 + lane;
-        const int32_t vc = (int32_t)clamp64(vfast[u], 0, p.capacity);
-        if (r < p.num_rows && vc > 0) {
-          const int b = r / p.rows_per_req;
-          atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
-        }
+        const int b = r / p.rows_per_req, i = r - b * p.rows_per_req;
+        const bool live = i < (int)clamp64(nfast[u], 0, p.rows_per_req);
+        const int32_t vc = live ? (int32_t)clamp64(vfast[u], 0, p.capacity) : 0;
+        if (r < p.num_rows && vc > 0) atomicMax(&gmax[b * p.groups_per_req + i / p.group_rows], vc);
       }
       __syncwarp();
       for (int g = lane; g < G; g += 32) pref[g] = (gmax[g] + kBM - 1) / kBM;
@@ -351,20 +355,20 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     // Per-group widest visible count and tile count from the visible counts
     // (device data, no host sync): every thread takes rows, four loads in flight.
     for (int r0 = 0; r0 < p.num_rows; r0 += 4 * kThreads) {
-      int32_t v[4];
+      int32_t v[4], nn[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int r = r0 + u * kThreads + threadIdx.x;
-        v[u] = r < p.num_rows ? __ldg(p.visible + r) : 0;
+        const int r = min(r0 + u * kThreads + (int)threadIdx.x, p.num_rows - 1);
+        v[u] = __ldg(p.visible + r);
+        nn[u] = p.next_n_lens != nullptr ? __ldg(p.next_n_lens + r / p.rows_per_req) : p.rows_per_req;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int r = r0 + u * kThreads + threadIdx.x;
-        const int32_t vc = (int32_t)clamp64(v[u], 0, p.capacity);
-        if (r < p.num_rows && vc > 0) {
-          const int b = r / p.rows_per_req;
-          atomicMax(&gmax[b * p.groups_per_req + (r - b * p.rows_per_req) / p.group_rows], vc);
-        }
+        const int b = r / p.rows_per_req, i = r - b * p.rows_per_req;
+        const bool live = i < (int)clamp64(nn[u], 0, p.rows_per_req);
+        const int32_t vc = live ? (int32_t)clamp64(v[u], 0, p.capacity) : 0;
+        if (r < p.num_rows && vc > 0) atomicMax(&gmax[b * p.groups_per_req + i / p.group_rows], vc);
       }
     }
     __syncthreads();
@@ -570,7 +574,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         r0 = b * p.rows_per_req + jj * p.group_rows;
         nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
         for (int i = et; i < nr * H; i += kEpiThreads) w_s[i] = p.weights[(int64_t)r0 * H + i];
-        for (int i = et; i < nr; i += kEpiThreads) vis_s[i] = (int32_t)clamp64(p.visible[r0 + i], 0, p.capacity);
+        for (int i = et; i < nr; i += kEpiThreads)
+          vis_s[i] = (int32_t)row_visible(p.visible, p.next_n_lens, r0 + i, p.rows_per_req, p.capacity);
         epi_bar(kEpiThreads);
         eg = g;
       }

@@ -16,14 +16,17 @@ from . import _abi
 def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Tensor,
                      block_table: torch.Tensor, visible_cols: torch.Tensor, *, page_cols: int,
                      out_cols: int, kv_dtype: int = _abi.KV_BF16, scale_offset: int = -1,
-                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                     out: Optional[torch.Tensor] = None, stream=None,
+                     next_n_lens: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Index logits fp32 [R, out_cols] (include/qsa.h, qsa_paged_mqa_logits).
 
     q: bf16 [R, H, 128]; weights: fp32 [R, H]; kv_cache: [num_pages, ...] paged
     keys whose dim-0 stride is the page stride; block_table: int32
     [num_requests, max_pages]; visible_cols: int32 [R].  For fp8 keys in the
     block-flat layout pass kv_dtype=KV_FP8_E4M3 and the byte offset of the
-    scales inside a block (page_cols * 128)."""
+    scales inside a block (page_cols * 128).  next_n_lens (int32
+    [num_requests]) selects qsa_paged_mqa_logits_ragged: a request's rows past
+    its count are -inf."""
     R, H, D = q.shape
     B, max_pages = block_table.shape
     if B == 0 or R % B:
@@ -40,7 +43,8 @@ def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Ten
         scale_stride = page_stride
     desc = _abi.make_desc(B, R // B, H, page_cols, max_pages, kv_cache.shape[0], out_cols, page_stride,
                           kv_dtype=kv_dtype, scale_page_stride=scale_stride, head_dim=D)
-    _abi.paged_mqa_logits(desc, q, weights, kv_cache, scales, block_table, visible_cols, out, stream)
+    _abi.paged_mqa_logits(desc, q, weights, kv_cache, scales, block_table, visible_cols, out, stream,
+                          next_n_lens=next_n_lens)
     return out
 
 

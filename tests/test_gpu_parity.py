@@ -60,7 +60,8 @@ def gpu_logits(inp, variant=qsa.VARIANT_AUTO, dev=None, stream=None):
     try:
         torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
                                    page_cols=s.page_cols, out_cols=s.out_cols, kv_dtype=s.kv_dtype,
-                                   scale_offset=inp.scale_offset, out=out, stream=stream)
+                                   scale_offset=inp.scale_offset, out=out, stream=stream,
+                                   next_n_lens=d.get("next_n_lens"))
         ran = qsa.last_variant()
     finally:
         qsa.force_variant(qsa.VARIANT_AUTO)
@@ -207,6 +208,81 @@ def test_cuda_graph_capture_and_replay(oracle_mod):
 
 
 # --------------------------------------------------------------------------
+# Ragged live rows (qsa_paged_mqa_logits_ragged)
+# --------------------------------------------------------------------------
+
+RAGGED = [
+    # (name, B, rows/req, H, page_cols, visible (cycled), out_cols, next_n_lens)
+    ("nn8_h4_p16", 5, 8, 4, 16, [700 + i for i in range(8)], 768, [1, 8, 0, 3, 11]),
+    ("nn4_h32_p64", 3, 4, 32, 64, [300, 301, 302, 303, 129, 130, 131, 132], 320, [2, 4, 1]),
+    ("nn2_h64_p64", 4, 2, 64, 64, [200, 201], 256, [1, 2, 0, 1]),
+    ("nn3_h3_page5", 2, 3, 3, 5, [41, 42, 43], 48, [2, 1]),  # CUDA-core scorer only
+]
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("case", RAGGED, ids=[c[0] for c in RAGGED])
+def test_ragged_rows_match_oracle(oracle_mod, case, kv_dtype, variant):
+    name, B, rpr, H, pc, vis, oc, nn = case
+    if kv_dtype == qi.KV_FP8 and (pc * 132) % 16:
+        pytest.skip("a block-flat fp8 page of this size is not 16-byte aligned")
+    R = B * rpr
+    spec = qi.custom(name, B, rpr, H, pc, (vis * R)[:R], oc, k=32, kv_dtype=kv_dtype, seed=77,
+                     next_n_lens=nn)
+    inp = qi.build_inputs(spec)
+    if not supported(inp, VARIANTS[variant]):
+        pytest.skip(f"{variant} does not serve this shape")
+    out, ran, d = gpu_logits(inp, VARIANTS[variant])
+    g = out.cpu().numpy()
+    assert_logits_match(g, oracle_mod.paged_mqa_logits(inp), kv_dtype, where=f"{name}/{variant}")
+    dead = ~spec.live_rows()
+    assert (g[dead].view(np.uint32) == 0xFF800000).all()
+    # the top-k of the live visible counts: dead rows select nothing
+    idx = gpu_topk(out, d["visible_live"], 32)
+    assert_topk_strict(idx, oracle_mod.select_topk(g, spec.live_visible(), 32), where=name)
+
+
+def test_ragged_dead_row_inputs_change_nothing():
+    """aiter #4221 test list: mutating padded Q rows must not change live logits."""
+    spec = qi.custom("dead", 4, 8, 4, 16, [500 + i for i in range(8)] * 4, 512, kv_dtype=qi.KV_BF16,
+                     seed=5, next_n_lens=[3, 8, 1, 5])
+    inp = qi.build_inputs(spec)
+    base, _, d = gpu_logits(inp)
+    dead = torch.from_numpy(~spec.live_rows()).cuda()
+    d["q"][dead] = 7.0
+    d["weights"][dead] = float("nan")
+    got, _, _ = gpu_logits(inp, dev=d)
+    assert torch.equal(got.view(torch.int32), base.view(torch.int32))
+
+
+def test_ragged_counts_rewritten_between_graph_replays(oracle_mod):
+    spec = qi.custom("ragged_graph", 3, 4, 4, 16, [300, 301, 302, 303] * 3, 320, seed=9,
+                     next_n_lens=[4, 4, 4])
+    inp = qi.build_inputs(spec)
+    d = qi.device_tensors(inp)
+    out = torch.empty((spec.num_rows, spec.out_cols), dtype=torch.float32, device="cuda")
+
+    def call():
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=spec.page_cols, out_cols=spec.out_cols, out=out,
+                                   next_n_lens=d["next_n_lens"])
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for nn in ([1, 2, 3], [0, 4, 2]):
+        d["next_n_lens"].copy_(torch.tensor(nn, dtype=torch.int32))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref = oracle_mod.paged_mqa_logits(inp, next_n_lens=np.array(nn, np.int32))
+        assert_logits_match(out.cpu().numpy(), ref, qi.KV_BF16, where=f"graph {nn}")
+
+
+# --------------------------------------------------------------------------
 # Top-k kernel on its own
 # --------------------------------------------------------------------------
 
@@ -326,7 +402,7 @@ def test_topk_visible_beyond_stride_is_clamped():
 # --------------------------------------------------------------------------
 
 FULL = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "fp8_h64", "prefill_chunk",
-        "mtp3_large_p64"]
+        "mtp3_large_p64", "ragged_nn8"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -339,16 +415,17 @@ def test_full_size_workload_sampled(oracle_mod, name):
     sub = out[torch.tensor(rows, device="cuda")].cpu().numpy()
     assert_logits_match(sub, ref, spec.kv_dtype, where=f"{name} rows {rows}")
     idx_t = nan_filled((spec.num_rows, spec.k), torch.int32, "cuda")
-    torch_api.select_topk(out, d["visible"], spec.k, out=idx_t)
+    vis_live = d.get("visible_live", d["visible"])  # ragged: dead rows select nothing
+    torch_api.select_topk(out, vis_live, spec.k, out=idx_t)
     torch.cuda.synchronize()
     idx = idx_t.cpu().numpy()
     # strict top-k on a bounded set of rows (the oracle sorts each row)
     trows = rows if spec.num_rows > 512 else list(range(spec.num_rows))
     g_rows = out[torch.tensor(trows, device="cuda")].cpu().numpy()
-    assert_topk_strict(idx[trows], oracle_mod.select_topk(g_rows, spec.visible[trows], spec.k), where=name)
-    assert_topk_within_tie_tolerance(idx[rows], ref, spec.visible[rows], spec.k, spec.kv_dtype, where=name)
+    assert_topk_strict(idx[trows], oracle_mod.select_topk(g_rows, spec.live_visible()[trows], spec.k), where=name)
+    assert_topk_within_tie_tolerance(idx[rows], ref, spec.live_visible()[rows], spec.k, spec.kv_dtype, where=name)
     # every masked entry of every row, bit-exact
-    vis_t = d["visible"].long()
+    vis_t = vis_live.long()
     cols = torch.arange(spec.out_cols, device="cuda")
     masked = cols[None, :] >= vis_t[:, None]
     bits = out.view(torch.int32)

@@ -298,6 +298,55 @@ def test_row_subset_matches_full_run(oracle_mod):
 
 
 # --------------------------------------------------------------------------
+# Ragged live rows (aiter #4221 "Ragged next_n for confidence-scheduled
+# verification": the leading next_n_lens[b] rows of a request are live, the
+# rest stay -inf; "mutating padded Q rows must not change live logits")
+# --------------------------------------------------------------------------
+
+
+def _ragged_spec(kv_dtype, nn):
+    vis = [90, 91, 92, 93, 17, 18, 19, 20, 60, 61, 62, 63, 33, 34, 35, 36]
+    return qi.custom("ragged", 4, 4, 4, 16, vis, 96, kv_dtype=kv_dtype, seed=41, next_n_lens=nn)
+
+
+@pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
+def test_ragged_rows_match_bruteforce_with_dead_rows_neg_inf(oracle_mod, kv_dtype):
+    nn = [0, 2, 4, 7]  # none live, two, all, more than the rows (all)
+    inp = qi.build_inputs(_ragged_spec(kv_dtype, nn))
+    got = oracle_mod.paged_mqa_logits(inp)
+    # brute force over every row (dense, no live-row rule), then the rule by hand
+    ref = brute.logits(inp)
+    for b, n in enumerate(nn):
+        for i in range(4):
+            if i >= min(n, 4):
+                ref[b * 4 + i, :] = -np.inf
+    assert _close_1ulp(got, ref)
+    assert np.isneginf(got[0:4]).all() and np.isneginf(got[6:8]).all()
+
+
+def test_ragged_dead_row_inputs_change_nothing(oracle_mod):
+    nn = [1, 3, 0, 2]
+    inp = qi.build_inputs(_ragged_spec(qi.KV_BF16, nn))
+    base = oracle_mod.paged_mqa_logits(inp)
+    live = inp.spec.live_rows()
+    q = inp.q.copy()
+    w = inp.weights.copy()
+    q[~live] = _int_bf16(np.full((int((~live).sum()), 4, 128), 3.0))
+    w[~live] = np.nan
+    vis = inp.spec.visible.copy()
+    vis[~live] = 96
+    got = oracle_mod.paged_mqa_logits(inp, q=q, weights=w, visible=vis)
+    assert (got.view(np.uint32) == base.view(np.uint32)).all()
+
+
+def test_ragged_full_counts_equal_the_uniform_call(oracle_mod):
+    inp = qi.build_inputs(_ragged_spec(qi.KV_BF16, [4, 4, 9, 4]))
+    got = oracle_mod.paged_mqa_logits(inp)
+    plain = oracle_mod.paged_mqa_logits(inp, next_n_lens=None)
+    assert (got.view(np.uint32) == plain.view(np.uint32)).all()
+
+
+# --------------------------------------------------------------------------
 # Top-k
 # --------------------------------------------------------------------------
 
