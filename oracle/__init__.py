@@ -61,6 +61,9 @@ def _load():
         lib.qsa_oracle_paged_mqa_logits.restype = ctypes.c_int
         lib.qsa_oracle_paged_mqa_logits.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i64, i64,
                                                     i64, vp, vp, vp, vp, vp, vp, vp, i64, vp, i32]
+        lib.qsa_oracle_paged_mqa_logits_ex.restype = ctypes.c_int
+        lib.qsa_oracle_paged_mqa_logits_ex.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i64, i64,
+                                                       i64, i32, vp, vp, vp, vp, vp, vp, vp, i64, vp, i32]
         lib.qsa_oracle_select_topk.restype = ctypes.c_int
         lib.qsa_oracle_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, i32]
         _lib = lib
@@ -94,7 +97,8 @@ def paged_mqa_logits(inp, rows: Optional[Sequence[int]] = None, threads: Optiona
     column of its other rows is -inf, i.e. those rows see no column."""
     lib = _load()
     s = inp.spec
-    q = np.ascontiguousarray(inp.q if q is None else q, dtype=np.uint16)
+    q_dtype = getattr(s, "q_dtype", 0)
+    q = np.ascontiguousarray(inp.q if q is None else q, dtype=np.uint16 if q_dtype == 0 else np.uint8)
     w = np.ascontiguousarray(inp.weights if weights is None else weights, dtype=np.float32)
     kvb = np.ascontiguousarray(inp.kv if kv is None else kv, dtype=np.uint8)
     bt = np.ascontiguousarray(inp.block_table if block_table is None else block_table, dtype=np.int32)
@@ -112,9 +116,9 @@ def paged_mqa_logits(inp, rows: Optional[Sequence[int]] = None, threads: Optiona
     scales = None
     if s.kv_dtype == 1:
         scales = ctypes.c_void_p(kvb.ctypes.data + inp.scale_offset)
-    st = lib.qsa_oracle_paged_mqa_logits(
+    st = lib.qsa_oracle_paged_mqa_logits_ex(
         s.num_requests, s.rows_per_req, s.num_heads, s.head_dim, s.page_cols, s.max_pages,
-        kvb.shape[0], s.kv_dtype, s.out_cols, inp.key_page_stride, inp.key_page_stride,
+        kvb.shape[0], s.kv_dtype, s.out_cols, inp.key_page_stride, inp.key_page_stride, q_dtype,
         _ptr(q), _ptr(w), _ptr(kvb), scales, _ptr(bt), _ptr(vis), _ptr(sel),
         n, _ptr(out), threads or default_threads())
     if st != 0:

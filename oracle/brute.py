@@ -2,8 +2,9 @@
 
 An independent restatement used to cross-check the C oracle: it de-pages each
 request's visible keys into a dense matrix with numpy fancy indexing, decodes
-bf16 by placing the 16 bits in the top half of a float32, decodes e4m3 with
-torch's float8_e4m3fn cast, and contracts with ``einsum`` in float64:
+bf16 by placing the 16 bits in the top half of a float32, decodes e4m3 (fp8
+keys, and fp8 q) with torch's float8_e4m3fn cast, and contracts with
+``einsum`` in float64:
 
     S[r, h, c] = sum_d q[r, h, d] * key[c, d]
     logit[r, c] = sum_h w[r, h] * max(S[r, h, c], 0)      for c < visible[r]
@@ -51,7 +52,7 @@ def logits(inp) -> np.ndarray:
     s = inp.spec
     R, out_cols = s.num_rows, s.out_cols
     out = np.full((R, out_cols), -np.inf, dtype=np.float32)
-    q = bf16_to_f64(inp.q)  # [R, H, D]
+    q = bf16_to_f64(inp.q) if getattr(s, "q_dtype", 0) == 0 else e4m3_to_f64(inp.q)  # [R, H, D]
     w = inp.weights.astype(np.float64)
     for b in range(s.num_requests):
         rows = range(b * s.rows_per_req, (b + 1) * s.rows_per_req)

@@ -15,6 +15,9 @@
  *                key[d]  = bf16(K[p][j][d])                   (bf16 cache)
  *                        | e4m3(K8[p][j][d]) * scale[p][j]    (fp8 cache)
  *                logit   = sum_h w[r][h] * max(0, sum_d q[r][h][d] * key[d])
+ *                q[r][h][d] = bf16(Q[r][h][d]), or e4m3(Q8[r][h][d]) with fp8 q
+ *                (aiter #4221 "Motivation": Q and K fp8 e4m3; weights, kv_scale and
+ *                the output fp32 - no separate q scale)
  *                (max(0, NaN) is NaN, as torch.relu: poisoned keys stay visible)
  *                rounded once to fp32; a zero result is stored as +0.0
  *
@@ -94,7 +97,8 @@ typedef struct {
   int32_t num_requests, rows_per_req, num_heads, head_dim, page_cols, max_pages, num_pages,
       kv_dtype;
   int64_t out_cols, key_page_stride, scale_page_stride;
-  const uint16_t* q;
+  int32_t q_dtype; /* 0: bf16 q, 1: e4m3 q */
+  const void* q;
   const float* weights;
   const uint8_t* kv;
   const uint8_t* scales;
@@ -138,9 +142,14 @@ static int oracle_row(const logits_job* J, int64_t r, float* out_row) {
     }
     double acc = 0.0;
     for (int64_t h = 0; h < H; ++h) {
-      const uint16_t* qh = J->q + (r * H + h) * D;
       double dot = 0.0;
-      for (int64_t d = 0; d < D; ++d) dot += qsa_oracle_bf16_value(qh[d]) * key[d];
+      if (J->q_dtype == 0) {
+        const uint16_t* qh = (const uint16_t*)J->q + (r * H + h) * D;
+        for (int64_t d = 0; d < D; ++d) dot += qsa_oracle_bf16_value(qh[d]) * key[d];
+      } else {
+        const uint8_t* qh = (const uint8_t*)J->q + (r * H + h) * D;
+        for (int64_t d = 0; d < D; ++d) dot += qsa_oracle_e4m3_value(qh[d]) * key[d];
+      }
       /* ReLU that lets NaN through, as torch.relu does: a poisoned key shows. */
       const double relu = dot < 0.0 ? 0.0 : dot;
       acc += (double)J->weights[r * H + h] * relu;
@@ -167,17 +176,19 @@ static void* logits_worker(void* arg) {
 }
 
 /* Logits of the selected rows (rows == NULL: every row, in order) into
- * out[num_sel][out_cols].  Returns 0, or non-zero on bad arguments / page ids. */
-int qsa_oracle_paged_mqa_logits(int32_t num_requests, int32_t rows_per_req, int32_t num_heads,
-                                int32_t head_dim, int32_t page_cols, int32_t max_pages,
-                                int32_t num_pages, int32_t kv_dtype, int64_t out_cols,
-                                int64_t key_page_stride, int64_t scale_page_stride,
-                                const uint16_t* q, const float* weights, const uint8_t* kv,
-                                const uint8_t* scales, const int32_t* block_table,
-                                const int32_t* visible, const int64_t* rows, int64_t num_sel,
-                                float* out, int32_t num_threads) {
+ * out[num_sel][out_cols], q bf16 (q_dtype 0) or e4m3 (q_dtype 1).  Returns 0,
+ * or non-zero on bad arguments / page ids. */
+int qsa_oracle_paged_mqa_logits_ex(int32_t num_requests, int32_t rows_per_req, int32_t num_heads,
+                                   int32_t head_dim, int32_t page_cols, int32_t max_pages,
+                                   int32_t num_pages, int32_t kv_dtype, int64_t out_cols,
+                                   int64_t key_page_stride, int64_t scale_page_stride, int32_t q_dtype,
+                                   const void* q, const float* weights, const uint8_t* kv,
+                                   const uint8_t* scales, const int32_t* block_table,
+                                   const int32_t* visible, const int64_t* rows, int64_t num_sel,
+                                   float* out, int32_t num_threads) {
   if (num_requests < 0 || rows_per_req < 1 || num_heads < 1 || head_dim < 1 || page_cols < 1 ||
-      max_pages < 1 || num_pages < 1 || out_cols < 0 || (kv_dtype != 0 && kv_dtype != 1))
+      max_pages < 1 || num_pages < 1 || out_cols < 0 || (kv_dtype != 0 && kv_dtype != 1) ||
+      (q_dtype != 0 && q_dtype != 1))
     return ORACLE_BAD_ARG;
   if (!q || !weights || !kv || !block_table || !visible || !out) return ORACLE_BAD_ARG;
   if (kv_dtype == 1 && !scales) return ORACLE_BAD_ARG;
@@ -195,7 +206,7 @@ int qsa_oracle_paged_mqa_logits(int32_t num_requests, int32_t rows_per_req, int3
   pthread_t tids[256];
   for (int t = 0; t < num_threads; ++t) {
     logits_job J = {num_requests, rows_per_req, num_heads, head_dim, page_cols, max_pages,
-                    num_pages, kv_dtype, out_cols, key_page_stride, scale_page_stride, q,
+                    num_pages, kv_dtype, out_cols, key_page_stride, scale_page_stride, q_dtype, q,
                     weights, kv, scales, block_table, visible, rows, num_sel, out,
                     num_threads, t, ORACLE_OK};
     jobs[t] = J;
@@ -211,6 +222,21 @@ int qsa_oracle_paged_mqa_logits(int32_t num_requests, int32_t rows_per_req, int3
     if (jobs[t].status != ORACLE_OK) status = jobs[t].status;
   }
   return status;
+}
+
+/* The same with bf16 q. */
+int qsa_oracle_paged_mqa_logits(int32_t num_requests, int32_t rows_per_req, int32_t num_heads,
+                                int32_t head_dim, int32_t page_cols, int32_t max_pages,
+                                int32_t num_pages, int32_t kv_dtype, int64_t out_cols,
+                                int64_t key_page_stride, int64_t scale_page_stride,
+                                const uint16_t* q, const float* weights, const uint8_t* kv,
+                                const uint8_t* scales, const int32_t* block_table,
+                                const int32_t* visible, const int64_t* rows, int64_t num_sel,
+                                float* out, int32_t num_threads) {
+  return qsa_oracle_paged_mqa_logits_ex(num_requests, rows_per_req, num_heads, head_dim, page_cols,
+                                        max_pages, num_pages, kv_dtype, out_cols, key_page_stride,
+                                        scale_page_stride, 0, q, weights, kv, scales, block_table,
+                                        visible, rows, num_sel, out, num_threads);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -36,6 +36,8 @@ import numpy as np
 HEAD_DIM = 128
 KV_BF16 = 0
 KV_FP8 = 1
+Q_BF16 = 0
+Q_FP8 = 1
 BF16_NAN_BITS = 0x7FC0
 FP8_NAN_CODE = 0x7F
 # Rows of a given config are drawn from seed BASE_SEED + config index.
@@ -76,6 +78,7 @@ class Spec:
     head_dim: int = HEAD_DIM
     max_pages: Optional[int] = None  # block-table row width; default covers out_cols
     next_n_lens: Optional[np.ndarray] = None  # int32 [B] live rows per request (ragged call), or None
+    q_dtype: int = Q_BF16  # Q_FP8: q as e4m3 codes (fp8 keys only)
 
     def __post_init__(self):
         self.visible = np.ascontiguousarray(self.visible, dtype=np.int32)
@@ -119,7 +122,7 @@ class Spec:
 @dataclasses.dataclass
 class Inputs:
     spec: Spec
-    q: np.ndarray  # uint16 bf16 bits [R, H, D]
+    q: np.ndarray  # uint16 bf16 bits, or uint8 e4m3 codes (fp8 q), [R, H, D]
     weights: np.ndarray  # float32 [R, H]
     kv: np.ndarray  # uint8 [num_pages, key_page_stride] raw paged cache
     key_page_stride: int  # bytes between pages (blocks)
@@ -146,7 +149,10 @@ def build_inputs(spec: Spec, rng: Optional[np.random.Generator] = None) -> Input
     total_needed = int(needed.sum())
     num_pages = total_needed + 1  # + one poison page
 
-    q = _bf16_bits(rng.standard_normal((R, H, D), dtype=np.float32))
+    if spec.q_dtype == Q_BF16:
+        q = _bf16_bits(rng.standard_normal((R, H, D), dtype=np.float32))
+    else:  # e4m3 codes of N(0,1) draws (no q scale: the weights carry it)
+        q = _e4m3_codes(rng.standard_normal((R, H, D), dtype=np.float32))
     weights = rng.random((R, H), dtype=np.float32)
 
     perm = rng.permutation(num_pages).astype(np.int32)
@@ -268,6 +274,13 @@ def ragged_nn8() -> Spec:
                 next_n_lens=nn)
 
 
+def fp8q_h64() -> Spec:
+    """fp8_h64 with fp8 q: 16 requests x 1 row, 32,768 columns, 64 heads, q and keys e4m3."""
+    vis = np.full(16, 32768, dtype=np.int32)
+    return Spec("fp8q_h64_16x1_kv32k_kvb64", 16, 1, 64, 64, 32768, 2048, KV_FP8, vis, BASE_SEED + 3,
+                q_dtype=Q_FP8)
+
+
 WORKLOADS = {
     "tiny_mtp": tiny_mtp,
     "single_row_decode": single_row_decode,
@@ -278,17 +291,19 @@ WORKLOADS = {
     "fp8_h64": fp8_h64,
     "prefill_chunk": prefill_chunk,
     "ragged_nn8": ragged_nn8,
+    "fp8q_h64": fp8q_h64,
 }
 
 
 def custom(name: str, num_requests: int, rows_per_req: int, num_heads: int, page_cols: int,
            visible: Sequence[int], out_cols: int, k: int = 64, kv_dtype: int = KV_BF16,
            seed: int = 7, max_pages: Optional[int] = None,
-           next_n_lens: Optional[Sequence[int]] = None) -> Spec:
+           next_n_lens: Optional[Sequence[int]] = None, q_dtype: int = Q_BF16) -> Spec:
     """Small ad-hoc shapes for tests."""
     nn = None if next_n_lens is None else np.asarray(next_n_lens, dtype=np.int32)
     return Spec(name, num_requests, rows_per_req, num_heads, page_cols, out_cols, k, kv_dtype,
-                np.asarray(visible, dtype=np.int32), seed, max_pages=max_pages, next_n_lens=nn)
+                np.asarray(visible, dtype=np.int32), seed, max_pages=max_pages, next_n_lens=nn,
+                q_dtype=q_dtype)
 
 
 def random_logit_rows(rng: np.random.Generator, num_rows: int, width: int,
@@ -332,7 +347,8 @@ def device_tensors(inp: Inputs, device="cuda", pin: bool = False) -> dict:
         return x.pin_memory() if pin else x.to(device)
 
     d = {
-        "q": t(inp.q.view(np.int16)).view(torch.bfloat16),
+        "q": (t(inp.q.view(np.int16)).view(torch.bfloat16) if inp.spec.q_dtype == Q_BF16
+              else t(inp.q).view(torch.float8_e4m3fn)),
         "weights": t(inp.weights),
         "kv": t(inp.kv),
         "block_table": t(inp.block_table),

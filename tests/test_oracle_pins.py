@@ -298,6 +298,34 @@ def test_row_subset_matches_full_run(oracle_mod):
 
 
 # --------------------------------------------------------------------------
+# fp8 q (aiter #4221 "Motivation": Q and K fp8 e4m3, weights and kv_scale f32)
+# --------------------------------------------------------------------------
+
+
+def _q8_spec(seed=3):
+    return qi.custom("q8", 3, 2, 8, 64, [130, 131, 64, 65, 1, 0], 192, kv_dtype=qi.KV_FP8, seed=seed,
+                     q_dtype=qi.Q_FP8)
+
+
+def test_fp8_q_equals_bf16_q_of_the_same_values(oracle_mod):
+    """Every finite e4m3 value is exact in bf16, so the fp8-q oracle must equal
+    the (separately pinned) bf16-q oracle on the decoded values, bit for bit."""
+    inp = qi.build_inputs(_q8_spec())
+    got = oracle_mod.paged_mqa_logits(inp)
+    as_bf16 = torch.from_numpy(inp.q).view(torch.float8_e4m3fn).to(torch.bfloat16)
+    inp16 = qi.build_inputs(_q8_spec())
+    inp16.spec.q_dtype = qi.Q_BF16
+    inp16.q = as_bf16.view(torch.int16).numpy().view(np.uint16)
+    ref = oracle_mod.paged_mqa_logits(inp16)
+    assert (got.view(np.uint32) == ref.view(np.uint32)).all()
+
+
+def test_fp8_q_matches_numpy_bruteforce(oracle_mod):
+    inp = qi.build_inputs(_q8_spec(seed=4))
+    assert _close_1ulp(oracle_mod.paged_mqa_logits(inp), brute.logits(inp))
+
+
+# --------------------------------------------------------------------------
 # Ragged live rows (aiter #4221 "Ragged next_n for confidence-scheduled
 # verification": the leading next_n_lens[b] rows of a request are live, the
 # rest stay -inf; "mutating padded Q rows must not change live logits")
