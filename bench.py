@@ -21,6 +21,7 @@ its own replica of the workload (weak scaling, no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -220,7 +221,7 @@ def oracle_sample_run(inp, requests, threads):
     lg = oracle.paged_mqa_logits(inp, rows=rows, threads=threads)
     oracle.select_topk(lg, spec.live_visible()[rows], spec.k, threads=threads)
     dt = time.perf_counter() - t0
-    vis = spec.visible.reshape(spec.num_requests, spec.rows_per_req).max(axis=1)
+    vis = spec.live_visible().reshape(spec.num_requests, spec.rows_per_req).max(axis=1)
     key_bytes = int(sum(int(vis[b]) for b in requests)) * spec.key_bytes_per_col
     return dt, key_bytes, len(rows)
 
@@ -310,8 +311,11 @@ def workload_config(spec: qi.Spec, l2_note):
     cfg = {"workload": spec.name, "requests": spec.num_requests, "rows_per_req": spec.rows_per_req,
            "heads": spec.num_heads, "head_dim": spec.head_dim, "page_cols": spec.page_cols,
            "out_cols": spec.out_cols, "k": spec.k, "kv": "bf16" if spec.kv_dtype == qi.KV_BF16 else "fp8_e4m3",
-           "visible_cols_total": int(spec.visible.astype(np.int64).sum()),
+           "q": "bf16" if spec.q_dtype == qi.Q_BF16 else "fp8_e4m3",
+           "visible_cols_total": int(spec.live_visible().astype(np.int64).sum()),
            "key_bytes_per_step": spec.key_bytes_touched()}
+    if spec.next_n_lens is not None:
+        cfg["live_rows"] = int(spec.live_rows().sum())
     if l2_note:
         cfg["l2"] = l2_note
     return cfg
@@ -341,9 +345,7 @@ def run_gpu(args):
         qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA}[args.variant])
 
     base = qi.WORKLOADS[args.workload]()
-    spec = qi.Spec(base.name, base.num_requests, base.rows_per_req, base.num_heads, base.page_cols,
-                   base.out_cols, base.k, base.kv_dtype, base.visible, base.seed + 7919 * rank,
-                   max_pages=base.max_pages)
+    spec = dataclasses.replace(base, seed=base.seed + 7919 * rank)  # per-rank data, same shape
     inp = qi.build_inputs(spec)
     host = qi.device_tensors(inp, pin=True)
     R, k = spec.num_rows, spec.k
@@ -498,7 +500,8 @@ def run_gpu(args):
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if spec.kv_dtype == qi.KV_BF16 else "fp8e4m3-keys/bf16-q",
+            "vs_baseline": None, "dtype": ("bf16" if spec.kv_dtype == qi.KV_BF16 else
+                                           "fp8e4m3-keys/bf16-q" if spec.q_dtype == qi.Q_BF16 else "fp8e4m3"),
             "data": "synthetic (seeded; shapes of the pages' workloads)",
             "config": workload_config(spec, l2_note),
             "variant": variant,

@@ -138,6 +138,25 @@ qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* desc, const void* q
                                        const int32_t* block_table, const int32_t* visible_cols,
                                        const int32_t* next_n_lens, float* out_logits, void* stream);
 
+/* q element types of qsa_paged_mqa_logits_ex. */
+typedef enum { QSA_Q_BF16 = 0, QSA_Q_FP8_E4M3 = 1 } qsa_q_dtype;
+
+/*
+ * qsa_paged_mqa_logits_ex - qsa_paged_mqa_logits_ragged with the q element type
+ * given.  With QSA_Q_FP8_E4M3 (aiter #4221 "Motivation": Q and K fp8 e4m3;
+ * weights, kv_scale and the output fp32 - no separate q scale, the weights
+ * carry it) q is OCP e4m3fn codes [R][H][D], 16-byte aligned, and the keys
+ * must be fp8 too (QSA_KV_FP8_E4M3; bf16 keys with fp8 q are rejected as mixed
+ * operand types); the definition is qsa_paged_mqa_logits's with
+ * q[r][h][d] = e4m3(Q8[r][h][d]).  The tcgen05 scorer multiplies the raw fp8
+ * q and keys (products exact, fp32 accumulation); the tolerance of fp8 keys
+ * applies.  QSA_Q_BF16 is qsa_paged_mqa_logits_ragged.
+ */
+qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* desc, int32_t q_dtype, const void* q,
+                                   const float* weights, const void* kv_cache, const float* scales,
+                                   const int32_t* block_table, const int32_t* visible_cols,
+                                   const int32_t* next_n_lens, float* out_logits, void* stream);
+
 /*
  * qsa_select_topk - per-row top-k column indices of a logits matrix.
  *

@@ -4,14 +4,14 @@ The compute lives in libqsa.so (CUDA kernels behind the C ABI in include/qsa.h);
 this package is its thin Python binding plus a device-side convenience layer
 (:mod:`.device`) that moves seeded host inputs into torch-owned GPU memory.
 """
-from ._abi import (EXPORTED, KV_BF16, KV_FP8_E4M3, LIB_PATH, QSA_ERR_CUDA, QSA_ERR_INVALID_ARG,
+from ._abi import (EXPORTED, KV_BF16, KV_FP8_E4M3, LIB_PATH, Q_BF16, Q_FP8_E4M3, QSA_ERR_CUDA, QSA_ERR_INVALID_ARG,
                    QSA_ERR_UNSUPPORTED, QSA_OK, VARIANT_AUTO, VARIANT_NAMES, VARIANT_ROWCORE,
                    VARIANT_UMMA, PagedDesc, QSAError, abi_version, device_status, force_variant, last_error,
                    last_variant, load_library, make_desc, paged_mqa_logits, plan_variant,
                    select_topk, status_string)
 
 __all__ = [
-    "EXPORTED", "KV_BF16", "KV_FP8_E4M3", "LIB_PATH", "QSA_OK", "QSA_ERR_INVALID_ARG", "QSA_ERR_UNSUPPORTED",
+    "EXPORTED", "KV_BF16", "KV_FP8_E4M3", "LIB_PATH", "Q_BF16", "Q_FP8_E4M3", "QSA_OK", "QSA_ERR_INVALID_ARG", "QSA_ERR_UNSUPPORTED",
     "QSA_ERR_CUDA", "VARIANT_AUTO", "VARIANT_ROWCORE", "VARIANT_UMMA", "VARIANT_NAMES", "PagedDesc", "QSAError",
     "abi_version", "device_status", "force_variant", "last_error", "last_variant", "load_library", "make_desc",
     "paged_mqa_logits", "plan_variant", "select_topk", "status_string",

@@ -16,11 +16,12 @@ LIB_PATH = os.path.join(_PKG, "libqsa.so")
 
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 KV_BF16, KV_FP8_E4M3 = 0, 1
+Q_BF16, Q_FP8_E4M3 = 0, 1
 VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA = -1, 0, 1
 VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma"}
 
 # Every symbol include/qsa.h declares.
-EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
@@ -60,6 +61,8 @@ def load_library():
         lib.qsa_paged_mqa_logits.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_paged_mqa_logits_ragged.restype = ctypes.c_int
         lib.qsa_paged_mqa_logits_ragged.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_paged_mqa_logits_ex.restype = ctypes.c_int
+        lib.qsa_paged_mqa_logits_ex.argtypes = [ctypes.POINTER(PagedDesc), i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_select_topk.restype = ctypes.c_int
         lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         lib.qsa_plan_variant.restype = ctypes.c_int
@@ -119,9 +122,14 @@ def make_desc(num_requests, rows_per_req, num_heads, page_cols, max_pages, num_p
 
 
 def paged_mqa_logits(desc: PagedDesc, q, weights, kv_cache, scales, block_table, visible_cols,
-                     out_logits, stream=None, next_n_lens=None) -> None:
+                     out_logits, stream=None, next_n_lens=None, q_dtype: int = Q_BF16) -> None:
     lib = load_library()
-    if next_n_lens is None:
+    if q_dtype != Q_BF16:
+        st = lib.qsa_paged_mqa_logits_ex(ctypes.byref(desc), int(q_dtype), _addr(q), _addr(weights),
+                                         _addr(kv_cache), _addr(scales), _addr(block_table),
+                                         _addr(visible_cols), _addr(next_n_lens), _addr(out_logits),
+                                         _stream(stream))
+    elif next_n_lens is None:
         st = lib.qsa_paged_mqa_logits(ctypes.byref(desc), _addr(q), _addr(weights), _addr(kv_cache),
                                       _addr(scales), _addr(block_table), _addr(visible_cols),
                                       _addr(out_logits), _stream(stream))

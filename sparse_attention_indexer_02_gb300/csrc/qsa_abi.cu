@@ -138,10 +138,22 @@ qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* d, const void* q, c
                                        const void* kv_cache, const float* scales,
                                        const int32_t* block_table, const int32_t* visible_cols,
                                        const int32_t* next_n_lens, float* out_logits, void* stream) {
+  return qsa_paged_mqa_logits_ex(d, QSA_Q_BF16, q, weights, kv_cache, scales, block_table, visible_cols,
+                                 next_n_lens, out_logits, stream);
+}
+
+qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* d, int32_t q_dtype, const void* q,
+                                   const float* weights, const void* kv_cache, const float* scales,
+                                   const int32_t* block_table, const int32_t* visible_cols,
+                                   const int32_t* next_n_lens, float* out_logits, void* stream) {
   qsa_status st = validate_desc(d);
   if (st != QSA_OK) return st;
   const int64_t rows = (int64_t)d->num_requests * d->rows_per_req;
   const bool fp8 = d->kv_dtype == QSA_KV_FP8_E4M3;
+  if (q_dtype != QSA_Q_BF16 && q_dtype != QSA_Q_FP8_E4M3)
+    return fail(QSA_ERR_INVALID_ARG, "q_dtype must be QSA_Q_BF16 or QSA_Q_FP8_E4M3 (got %d)", q_dtype);
+  const bool q8 = q_dtype == QSA_Q_FP8_E4M3;
+  if (q8 && !fp8) return fail(QSA_ERR_INVALID_ARG, "fp8 q needs fp8 keys (mixed operand types)");
   if (fp8 && !scales) return fail(QSA_ERR_INVALID_ARG, "fp8 keys need a scales pointer");
   if (!fp8 && scales) return fail(QSA_ERR_INVALID_ARG, "bf16 keys take no scales (mixed operand types)");
   if (rows == 0 || d->out_cols == 0) {
@@ -188,6 +200,7 @@ qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* d, const void* q, c
   p.max_pages = d->max_pages;
   p.num_pages = d->num_pages;
   p.fp8 = fp8 ? 1 : 0;
+  p.q8 = q8 ? 1 : 0;
 
   const char* msg = "launch failed";
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -10,7 +10,7 @@ namespace qsa {
 
 // Parameters of one scoring launch, resolved on the host from qsa_paged_desc.
 struct ScoreParams {
-  const uint16_t* q;        // bf16 bits [R][H][128]
+  const uint16_t* q;        // bf16 bits [R][H][128], or e4m3 codes when q8
   const float* weights;     // [R][H]
   const uint8_t* kv;        // paged keys
   const uint8_t* scales;    // fp8 scales base (NULL for bf16)
@@ -24,6 +24,7 @@ struct ScoreParams {
   int64_t capacity;         // min(out_cols, max_pages * page_cols): largest legal visible count
   int32_t num_requests, rows_per_req, num_rows, num_heads, page_cols, max_pages, num_pages;
   int32_t fp8;
+  int32_t q8;               // q as e4m3 codes [R][H][128] (fp8 keys only)
 };
 
 // Each launcher returns cudaSuccess or the launch error; `msg` gets a reason

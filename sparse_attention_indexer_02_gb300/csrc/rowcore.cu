@@ -134,8 +134,13 @@ __global__ void __launch_bounds__(kThreads, HR >= 8 ? 1 : 2) rowcore_kernel(cons
     const int h = i / kHeadDim;
     float v = 0.0f;
     if (h < p.num_heads) {
-      const uint32_t bits = p.q[(row * p.num_heads) * kHeadDim + i];
-      v = __uint_as_float(bits << 16);
+      if (p.q8) {  // e4m3 code -> half (exact) -> float
+        const uint8_t code = reinterpret_cast<const uint8_t*>(p.q)[(row * p.num_heads) * kHeadDim + i];
+        v = __half2float(__half(__nv_cvt_fp8_to_halfraw(code, __NV_E4M3)));
+      } else {
+        const uint32_t bits = p.q[(row * p.num_heads) * kHeadDim + i];
+        v = __uint_as_float(bits << 16);
+      }
     }
     q_s[i] = v;
   }

@@ -182,13 +182,15 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
     }
   }
   {
+    // bf16 q: 64-element (128-byte) K-halves; fp8 q: one 128-byte row of D codes
     cuuint64_t dims[2] = {128, (cuuint64_t)p.num_rows * (cuuint64_t)p.num_heads};
-    cuuint64_t strides[1] = {256};
-    cuuint32_t box[2] = {64, (cuuint32_t)N};
+    cuuint64_t strides[1] = {(cuuint64_t)(p.q8 ? 128 : 256)};
+    cuuint32_t box[2] = {(cuuint32_t)(p.q8 ? 128 : 64), (cuuint32_t)N};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box,
-                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(&q_map, p.q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<uint16_t*>(p.q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
       *msg = "q tensor map rejected by the driver";
       return cudaErrorInvalidValue;
@@ -199,7 +201,9 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   if (e != cudaSuccess) return e;
   const int64_t upper = (int64_t)up.num_groups * up.tiles_cap;
   const int grid = (int)(upper < info.num_sms ? (upper < 1 ? 1 : upper) : info.num_sms);
-  const Layout L = make_layout(N, up.num_groups, p.fp8 != 0);
+  const int kind = !p.fp8 ? kKindBf16 : (p.q8 ? kKindFp8Q : kKindFp8Keys);
+  const Layout L = make_layout(N, up.num_groups, kind);
+  if (kind == kKindFp8Q) return launch_q8(p.num_heads, kv_map, q_map, up, L, grid, stream);
   return p.fp8 ? launch_fp8(p.num_heads, kv_map, q_map, up, L, grid, stream)
                : launch_bf16(p.num_heads, kv_map, q_map, up, L, grid, stream);
 }

@@ -6,7 +6,7 @@ namespace umma {
 
 cudaError_t launch_fp8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                        const Layout& L, int grid, cudaStream_t s) {
-  return launch_any<true>(heads, kv, qm, up, L, grid, s);
+  return launch_any<kKindFp8Keys>(heads, kv, qm, up, L, grid, s);
 }
 
 }  // namespace umma

@@ -39,6 +39,9 @@
 namespace qsa {
 namespace umma {
 
+constexpr int kKindBf16 = 0;                // bf16 keys, bf16 q
+constexpr int kKindFp8Keys = 1;             // fp8 keys widened to bf16 in shared memory, bf16 q
+constexpr int kKindFp8Q = 2;                // fp8 keys, fp8 q: kind::f8f6f4 MMA
 constexpr int kBM = 128;                    // keys per tile (MMA M)
 constexpr int kHalfBytes = kBM * 128;       // one 64-element K-half of a bf16 key tile
 constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB
@@ -50,11 +53,11 @@ constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (s
 // quadrant for bf16 keys, one for fp8), then 8 fp8->bf16 converter warps
 // (fp8) or 4 spare warps that only take part in the CTA-wide barriers (bf16:
 // ptxas 13.0 for aarch64 hosts crashes on this kernel without them).
-template <bool FP8>
+template <bool CONV>
 struct Roles {
-  static constexpr int kEpiWarps = FP8 ? 4 : 8;
+  static constexpr int kEpiWarps = CONV ? 4 : 8;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kConvWarps = FP8 ? 8 : 4;
+  static constexpr int kConvWarps = CONV ? 8 : 4;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 };
@@ -94,14 +97,15 @@ struct Layout {
   int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, total;
 };
 
-inline Layout make_layout(int N, int groups, bool fp8) {
+inline Layout make_layout(int N, int groups, int kind) {
+  const bool fp8 = kind != kKindBf16, conv = kind == kKindFp8Keys;
   Layout L;
   L.n = N;
   L.tmem_cols = 2 * N < 32 ? 32 : 2 * N;
-  L.idesc = ptx::idesc_bf16_f32(kBM, N);
+  L.idesc = kind == kKindFp8Q ? ptx::idesc_e4m3_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N);
   L.stage_bytes = fp8 ? kFp8StageAlloc : kTileBytes;
-  L.a_stages = fp8 ? kFp8ConvStages : 0;
-  const int ring = fp8 ? kScaleRing * kBM * 4 : 0;
+  L.a_stages = conv ? kFp8ConvStages : 0;
+  const int ring = conv ? kScaleRing * kBM * 4 : 0;
   const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 +
                    8 * (groups + 1);
   int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
@@ -110,7 +114,7 @@ inline Layout make_layout(int N, int groups, bool fp8) {
   L.b_off = L.a_off + L.a_stages * kTileBytes;
   L.ring_off = L.b_off + N * 256;      // fp8 only: per-tile key scales
   L.bar_off = L.ring_off + ring;
-  const int nbars = 2 * L.stages + 2 * L.a_stages + (fp8 ? kScaleRing : 0) + 2 + 2 + 4;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + (conv ? kScaleRing : 0) + 2 + 2 + 4;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4;        // pref[G + 1], gmax[G]
@@ -230,11 +234,14 @@ __device__ __forceinline__ void fill_tail(const UmmaParams& p, const int32_t* pr
   }
 }
 
-template <int H, bool FP8>
-__global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
+template <int H, int KIND>
+__global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     umma_score_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const UmmaParams p, const Layout L) {
-  using R = Roles<FP8>;
+  constexpr bool FP8 = KIND != kKindBf16;      // fp8 keys (+ per-key scales)
+  constexpr bool CONV = KIND == kKindFp8Keys;  // widened to bf16 by the converter warps
+  constexpr bool Q8 = KIND == kKindFp8Q;       // fp8 q: e4m3 x e4m3 MMA on the copied keys
+  using R = Roles<CONV>;
   constexpr int kThreads = R::kThreads;
   constexpr int kEpiThreads = R::kEpiThreads;
   extern __shared__ uint8_t smem_raw[];
@@ -243,14 +250,14 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   const int kAStages = L.a_stages;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* S = smem;                          // TMA stages
-  uint8_t* A = FP8 ? smem + L.a_off : smem;   // MMA A-operand stages (bf16, 128-byte swizzle)
+  uint8_t* A = CONV ? smem + L.a_off : smem;  // MMA A-operand stages (128-byte swizzle)
   uint8_t* Bq = smem + L.b_off;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
   uint64_t* empty = full + kStages;
   uint64_t* afull = empty + kStages;          // fp8: converter -> MMA
   uint64_t* aempty = afull + kAStages;        // fp8: MMA -> converter
   uint64_t* sfull = aempty + kAStages;        // fp8: converter -> epilogue, one per scale slot
-  uint64_t* tfull = sfull + (FP8 ? kScaleRing : 0);
+  uint64_t* tfull = sfull + (CONV ? kScaleRing : 0);
   float* scale_ring = reinterpret_cast<float*>(smem + L.ring_off);  // fp8: [kScaleRing][128]
   uint64_t* tempty = tfull + 2;
   uint64_t* qfull = tempty + 2;
@@ -275,13 +282,15 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&empty[s], FP8 ? R::kConvThreads : 1);
+      // freed by the converter (widened keys), or by the MMA and - fp8 q: the
+      // epilogue reads each key's scale from the stage - every epilogue thread
+      ptx::mbar_init(&empty[s], CONV ? R::kConvThreads : (Q8 ? 1 + kEpiThreads : 1));
     }
     for (int s = 0; s < kAStages; ++s) {
       ptx::mbar_init(&afull[s], R::kConvThreads);
       ptx::mbar_init(&aempty[s], 1);
     }
-    if (FP8)
+    if (CONV)
       for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], kBM);
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
@@ -441,9 +450,14 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           if (q_loads > 0) ok = wait_phase(qempty, (q_loads - 1) & 1, abort_flag, p.fault);
           if (!ok) break;
           if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(qfull, 2u * N * 128u);
-            ptx::tma_load_2d(Bq, &q_map, 0, r0 * H, qfull);
-            ptx::tma_load_2d(Bq + N * 128, &q_map, 64, r0 * H, qfull);
+            if (Q8) {  // one 128-byte row (all of D) per row-head
+              ptx::mbar_arrive_expect_tx(qfull, (uint32_t)N * 128u);
+              ptx::tma_load_2d(Bq, &q_map, 0, r0 * H, qfull);
+            } else {  // two 64-element K-halves
+              ptx::mbar_arrive_expect_tx(qfull, 2u * N * 128u);
+              ptx::tma_load_2d(Bq, &q_map, 0, r0 * H, qfull);
+              ptx::tma_load_2d(Bq + N * 128, &q_map, 64, r0 * H, qfull);
+            }
           }
           qg = g;
           ++q_loads;
@@ -514,21 +528,32 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         ok = wait_phase(&tempty[acc], acc_phase ^ 1u, abort_flag, p.fault);
         if (!ok) break;
         ptx::tc_fence_after();
-        ok = wait_phase(FP8 ? &afull[stage] : &full[stage], phase, abort_flag, p.fault);
+        ok = wait_phase(CONV ? &afull[stage] : &full[stage], phase, abort_flag, p.fault);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * N);
-        const uint32_t a0 = a_base + stage * kTileBytes;
+        if (Q8) {
+          // the fp8 key rows as copied: 128 bytes (all of D) a key, 4 MMAs of K = 32
+          const uint32_t a0 = a_base + stage * (uint32_t)L.stage_bytes;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t koff = (uint32_t)(k & 3) * 32u;
-          const uint64_t ad = ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff);
-          const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
-          ptx::mma_bf16(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t ad = ptx::sw128_desc(a0 + (uint32_t)k * 32u);
+            const uint64_t bd = ptx::sw128_desc(b_base + (uint32_t)k * 32u);
+            ptx::mma_e4m3(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+          }
+        } else {
+          const uint32_t a0 = a_base + stage * kTileBytes;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t koff = (uint32_t)(k & 3) * 32u;
+            const uint64_t ad = ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff);
+            const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
+            ptx::mma_bf16(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+          }
         }
-        ptx::mma_commit(FP8 ? &aempty[stage] : &empty[stage]);
+        ptx::mma_commit(CONV ? &aempty[stage] : &empty[stage]);
         ptx::mma_commit(&tfull[acc]);
-        if (++stage == (FP8 ? kAStages : kStages)) {
+        if (++stage == (CONV ? kAStages : kStages)) {
           stage = 0;
           phase ^= 1u;
         }
@@ -584,11 +609,23 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       // for every s, so the sign goes inside the ReLU and |s| is applied once
       // per row after the head sum.
       float sgn = 1.0f, mag = 1.0f;
-      if (FP8) {
+      if (CONV) {
         const int i = t - t_begin;
         ok = wait_phase(&sfull[i % kScaleRing], (uint32_t)(i / kScaleRing) & 1u, abort_flag, p.fault);
         if (!ok) break;
         const float sc = scale_ring[(i % kScaleRing) * kBM + m];
+        sgn = sc < 0.0f ? -1.0f : 1.0f;
+        mag = fabsf(sc);
+      } else if (Q8) {
+        // the scale sits in the tile's TMA stage, which stays filled until this
+        // thread (and the MMA) release it; waiting on its completed fill orders
+        // the copied bytes for this thread
+        const int i = t - t_begin;
+        const int st = i % kStages;
+        ok = wait_phase(&full[st], (uint32_t)(i / kStages) & 1u, abort_flag, p.fault);
+        if (!ok) break;
+        const float sc = *reinterpret_cast<const float*>(S + st * L.stage_bytes + kFp8StageBytes + m * 4);
+        ptx::mbar_arrive(&empty[st]);
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
@@ -649,8 +686,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 
     // (2) fp8: this CTA's share of the -inf tail, after its tiles (the
     // converter warps are busy until then).  bf16: the spare warps write it.
-    if (FP8 && ok && setup_ok) fill_tail<kEpiThreads>(p, pref, G, total, et);
-  } else if (FP8) {
+    if (CONV && ok && setup_ok) fill_tail<kEpiThreads>(p, pref, G, total, et);
+  } else if (CONV) {
     // ------------------------------------------------------------ fp8 -> bf16 converter
     // Thread (m, kh) widens the kh-th 64-element half of key row m.  The TMA
     // stage holds 128-byte fp8 rows in the 128-byte swizzle (16-byte chunk j
@@ -711,7 +748,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     }
   }
 
-  if (!FP8 && warp >= 2 + R::kEpiWarps && setup_ok) {
+  if (!CONV && warp >= 2 + R::kEpiWarps && setup_ok) {
     // ------------------------------------------------------------ bf16 spare warps
     // the -inf tail, while the pipeline starts up and streams keys
     fill_tail<R::kConvThreads>(p, pref, G, total, (int)threadIdx.x - 64 - kEpiThreads);
@@ -727,18 +764,20 @@ cudaError_t launch_bf16(int heads, const CUtensorMap& kv, const CUtensorMap& qm,
                         const Layout& L, int grid, cudaStream_t s);
 cudaError_t launch_fp8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                        const Layout& L, int grid, cudaStream_t s);
+cudaError_t launch_q8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                      const Layout& L, int grid, cudaStream_t s);
 
-template <int H, bool FP8>
+template <int H, int KIND>
 cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up, const Layout& L,
                      int grid, cudaStream_t s) {
-  auto kern = umma_score_kernel<H, FP8>;
+  auto kern = umma_score_kernel<H, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
   // programmatic stream serialisation: the launch may begin while the
   // previous kernel finishes; the kernel waits for it before touching memory
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(Roles<FP8>::kThreads, 1, 1);
+  cfg.blockDim = dim3(Roles<KIND == kKindFp8Keys>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -751,17 +790,17 @@ cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaPar
   return cudaGetLastError();
 }
 
-template <bool FP8>
+template <int KIND>
 cudaError_t launch_any(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                        const Layout& L, int grid, cudaStream_t s) {
   switch (heads) {
-    case 1: return launch_h<1, FP8>(kv, qm, up, L, grid, s);
-    case 2: return launch_h<2, FP8>(kv, qm, up, L, grid, s);
-    case 4: return launch_h<4, FP8>(kv, qm, up, L, grid, s);
-    case 8: return launch_h<8, FP8>(kv, qm, up, L, grid, s);
-    case 16: return launch_h<16, FP8>(kv, qm, up, L, grid, s);
-    case 32: return launch_h<32, FP8>(kv, qm, up, L, grid, s);
-    default: return launch_h<64, FP8>(kv, qm, up, L, grid, s);
+    case 1: return launch_h<1, KIND>(kv, qm, up, L, grid, s);
+    case 2: return launch_h<2, KIND>(kv, qm, up, L, grid, s);
+    case 4: return launch_h<4, KIND>(kv, qm, up, L, grid, s);
+    case 8: return launch_h<8, KIND>(kv, qm, up, L, grid, s);
+    case 16: return launch_h<16, KIND>(kv, qm, up, L, grid, s);
+    case 32: return launch_h<32, KIND>(kv, qm, up, L, grid, s);
+    default: return launch_h<64, KIND>(kv, qm, up, L, grid, s);
   }
 }
 

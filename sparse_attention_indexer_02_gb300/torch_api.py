@@ -20,7 +20,8 @@ def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Ten
                      next_n_lens: Optional[torch.Tensor] = None) -> torch.Tensor:
     """Index logits fp32 [R, out_cols] (include/qsa.h, qsa_paged_mqa_logits).
 
-    q: bf16 [R, H, 128]; weights: fp32 [R, H]; kv_cache: [num_pages, ...] paged
+    q: bf16 [R, H, 128], or float8_e4m3fn (fp8 keys only: qsa_paged_mqa_logits_ex
+    with fp8 q); weights: fp32 [R, H]; kv_cache: [num_pages, ...] paged
     keys whose dim-0 stride is the page stride; block_table: int32
     [num_requests, max_pages]; visible_cols: int32 [R].  For fp8 keys in the
     block-flat layout pass kv_dtype=KV_FP8_E4M3 and the byte offset of the
@@ -43,8 +44,9 @@ def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Ten
         scale_stride = page_stride
     desc = _abi.make_desc(B, R // B, H, page_cols, max_pages, kv_cache.shape[0], out_cols, page_stride,
                           kv_dtype=kv_dtype, scale_page_stride=scale_stride, head_dim=D)
+    q_dtype = _abi.Q_FP8_E4M3 if q.dtype in (torch.float8_e4m3fn, torch.uint8) else _abi.Q_BF16
     _abi.paged_mqa_logits(desc, q, weights, kv_cache, scales, block_table, visible_cols, out, stream,
-                          next_n_lens=next_n_lens)
+                          next_n_lens=next_n_lens, q_dtype=q_dtype)
     return out
 
 

@@ -83,6 +83,17 @@ def test_mixed_operand_types_rejected(lib):
     assert e.value.status == qsa.QSA_ERR_INVALID_ARG
 
 
+def test_fp8_q_needs_fp8_keys_and_a_known_q_dtype(lib):
+    """fp8 q with bf16 keys is a mixed-operand call (SGLang #48649 rejects_mixed_operand_dtypes)."""
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.paged_mqa_logits(_desc(), 16, 16, 16, None, 16, 16, 16, stream=0, q_dtype=qsa.Q_FP8_E4M3)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "mixed" in str(e.value)
+    d8 = _desc(kv_dtype=qsa.KV_FP8_E4M3, key_page_stride=16 * 132, scale_page_stride=16 * 132)
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.paged_mqa_logits(d8, 16, 16, 16, 16, 16, 16, 16, stream=0, q_dtype=7)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "q_dtype" in str(e.value)
+
+
 def test_null_and_misaligned_pointers_rejected(lib):
     with pytest.raises(qsa.QSAError) as e:
         qsa.paged_mqa_logits(_desc(), None, 16, 16, None, 16, 16, 16, stream=0)

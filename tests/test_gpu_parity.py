@@ -208,6 +208,46 @@ def test_cuda_graph_capture_and_replay(oracle_mod):
 
 
 # --------------------------------------------------------------------------
+# fp8 q x fp8 keys (qsa_paged_mqa_logits_ex)
+# --------------------------------------------------------------------------
+
+Q8_CASES = [c for c in SMALL if (c[4] * 132) % 16 == 0]
+
+
+@pytest.mark.parametrize("variant", list(VARIANTS))
+@pytest.mark.parametrize("case", Q8_CASES, ids=[c[0] for c in Q8_CASES])
+def test_fp8_q_small_shapes_match_oracle(oracle_mod, case, variant):
+    name, B, rpr, H, pc, vis, oc, k = case
+    R = B * rpr
+    spec = qi.custom(name, B, rpr, H, pc, (vis * R)[:R], oc, k=k, kv_dtype=qi.KV_FP8, seed=321,
+                     q_dtype=qi.Q_FP8)
+    inp = qi.build_inputs(spec)
+    if not supported(inp, VARIANTS[variant]):
+        pytest.skip(f"{variant} does not serve this shape")
+    out, ran, d = gpu_logits(inp, VARIANTS[variant])
+    if variant != "auto":
+        assert ran == VARIANTS[variant]
+    g = out.cpu().numpy()
+    ref = oracle_mod.paged_mqa_logits(inp)
+    assert_logits_match(g, ref, qi.KV_FP8, where=f"q8 {name}/{variant}")
+    idx = gpu_topk(out, d["visible"], k)
+    assert_topk_strict(idx, oracle_mod.select_topk(g, spec.visible, k), where=name)
+
+
+@pytest.mark.parametrize("variant", ["rowcore", "umma"])
+def test_fp8_q_exact_integer_case_is_bit_exact(oracle_mod, variant):
+    """q and keys in {-3..3}, power-of-two scales and weights: exact in fp32."""
+    spec = qi.custom("exact_q8", 2, 4, 4, 16, [300, 301, 302, 303, 17, 18, 19, 0], 320,
+                     kv_dtype=qi.KV_FP8, seed=3, q_dtype=qi.Q_FP8)
+    inp, qv, _, _ = exact_case(qi.KV_FP8, spec)
+    inp.q = qi._e4m3_codes(qv.astype(np.float32))
+    out, ran, _ = gpu_logits(inp, VARIANTS[variant])
+    assert ran == VARIANTS[variant]
+    ref = oracle_mod.paged_mqa_logits(inp)
+    assert (out.cpu().numpy().view(np.uint32) == ref.view(np.uint32)).all()
+
+
+# --------------------------------------------------------------------------
 # Ragged live rows (qsa_paged_mqa_logits_ragged)
 # --------------------------------------------------------------------------
 
@@ -402,7 +442,7 @@ def test_topk_visible_beyond_stride_is_clamped():
 # --------------------------------------------------------------------------
 
 FULL = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "fp8_h64", "prefill_chunk",
-        "mtp3_large_p64", "ragged_nn8"]
+        "mtp3_large_p64", "ragged_nn8", "fp8q_h64"]
 
 
 @pytest.mark.parametrize("name", FULL)
