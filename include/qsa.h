@@ -143,9 +143,9 @@ typedef enum { QSA_Q_BF16 = 0, QSA_Q_FP8_E4M3 = 1 } qsa_q_dtype;
 
 /*
  * qsa_paged_mqa_logits_ex - qsa_paged_mqa_logits_ragged with the q element type
- * given.  With QSA_Q_FP8_E4M3 (aiter #4221 "Motivation": Q and K fp8 e4m3;
- * weights, kv_scale and the output fp32 - no separate q scale, the weights
- * carry it) q is OCP e4m3fn codes [R][H][D], 16-byte aligned, and the keys
+ * given.  With QSA_Q_FP8_E4M3 (aiter #4221 "Motivation": q and keys are e4m3
+ * codes, weights, key scales and logits fp32; q has no scale of its own, the
+ * weights carry it) q is OCP e4m3fn codes [R][H][D], 16-byte aligned, and the keys
  * must be fp8 too (QSA_KV_FP8_E4M3; bf16 keys with fp8 q are rejected as mixed
  * operand types); the definition is qsa_paged_mqa_logits's with
  * q[r][h][d] = e4m3(Q8[r][h][d]).  The tcgen05 scorer multiplies the raw fp8

@@ -16,8 +16,8 @@
  *                        | e4m3(K8[p][j][d]) * scale[p][j]    (fp8 cache)
  *                logit   = sum_h w[r][h] * max(0, sum_d q[r][h][d] * key[d])
  *                q[r][h][d] = bf16(Q[r][h][d]), or e4m3(Q8[r][h][d]) with fp8 q
- *                (aiter #4221 "Motivation": Q and K fp8 e4m3; weights, kv_scale and
- *                the output fp32 - no separate q scale)
+ *                (aiter #4221 "Motivation": both q and the keys are e4m3 codes while
+ *                the weights, key scales and logits stay fp32; q has no scale of its own)
  *                (max(0, NaN) is NaN, as torch.relu: poisoned keys stay visible)
  *                rounded once to fp32; a zero result is stored as +0.0
  *

@@ -284,7 +284,8 @@ def test_ragged_rows_match_oracle(oracle_mod, case, kv_dtype, variant):
 
 
 def test_ragged_dead_row_inputs_change_nothing():
-    """aiter #4221 test list: mutating padded Q rows must not change live logits."""
+    """aiter #4221 "Test plan": editing the q of a request's rows past its live count
+    leaves every live logit as it was."""
     spec = qi.custom("dead", 4, 8, 4, 16, [500 + i for i in range(8)] * 4, 512, kv_dtype=qi.KV_BF16,
                      seed=5, next_n_lens=[3, 8, 1, 5])
     inp = qi.build_inputs(spec)

@@ -298,7 +298,7 @@ def test_row_subset_matches_full_run(oracle_mod):
 
 
 # --------------------------------------------------------------------------
-# fp8 q (aiter #4221 "Motivation": Q and K fp8 e4m3, weights and kv_scale f32)
+# fp8 q (aiter #4221 "Motivation": q and keys as e4m3 codes, weights and key scales fp32)
 # --------------------------------------------------------------------------
 
 
@@ -328,7 +328,8 @@ def test_fp8_q_matches_numpy_bruteforce(oracle_mod):
 # --------------------------------------------------------------------------
 # Ragged live rows (aiter #4221 "Ragged next_n for confidence-scheduled
 # verification": the leading next_n_lens[b] rows of a request are live, the
-# rest stay -inf; "mutating padded Q rows must not change live logits")
+# rest stay -inf; the page's test plan edits the q of dead rows and expects
+# no live logit to change)
 # --------------------------------------------------------------------------
 
 
