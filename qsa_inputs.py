@@ -264,14 +264,14 @@ def prefill_chunk() -> Spec:
 
 
 def ragged_nn8() -> Spec:
-    """aiter #4221 ragged mix: 116 requests x next_n 8, next_n_lens ~ U{1..8}, fp8
-    block-flat KV block 64, 32 heads, prompts ~ U[32K, 128K] tokens, k 2048."""
+    """aiter #4221 ragged mix: 116 requests x next_n 8, next_n_lens ~ U{1..8}, fp8 q and
+    fp8 block-flat keys (KV block 64), 32 heads, prompts ~ U[32K, 128K] tokens, k 2048."""
     rng = np.random.default_rng(BASE_SEED + 5)
     L = rng.integers(32768, 131072 + 1, size=116)
     nn = rng.integers(1, 8 + 1, size=116).astype(np.int32)
     vis = decode_visible(L.tolist(), 8)
-    return Spec("ragged_116x8_nn1-8_fp8_h32", 116, 8, 32, 64, 32832, 2048, KV_FP8, vis, BASE_SEED + 5,
-                next_n_lens=nn)
+    return Spec("ragged_116x8_nn1-8_fp8q_h32", 116, 8, 32, 64, 32832, 2048, KV_FP8, vis, BASE_SEED + 5,
+                next_n_lens=nn, q_dtype=Q_FP8)
 
 
 def fp8q_h64() -> Spec:

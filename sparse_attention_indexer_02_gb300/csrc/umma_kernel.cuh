@@ -23,10 +23,10 @@
 //    q is loaded by a 2-D tensor copy once the previous group's MMAs are done.
 //  * warp 1 (MMA): one thread issues 8 tcgen05.mma (K = 16 each) per tile into
 //    one of two TMEM accumulators and commits the stage back to the producer.
-//  * warps 2-9 (epilogue, two warps per TMEM lane quadrant, each taking
-//    alternate row blocks of the group): tcgen05.ld of the tile's columns,
-//    per head ReLU * weight, head sum, +0.0, -inf past the row's visible
-//    count, store.
+//  * warps 2-13 (epilogue, three warps per TMEM lane quadrant, each taking
+//    every third row block of the group; four warps with the converter):
+//    tcgen05.ld of the tile's columns, per head ReLU * weight, head sum,
+//    +0.0, -inf past the row's visible count, store.
 // Every barrier wait gives up after about a second, sets the device fault
 // word (qsa_device_status) and lets the CTA drain and exit.
 #pragma once
@@ -49,15 +49,15 @@ constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
 constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
 constexpr int kFp8StageAlloc = kFp8StageBytes + 1024;  // + the block's 128 fp32 scales, 1024-aligned
 constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (see the converter)
-// Warp roles: 0 TMA, 1 MMA, then the epilogue warps (two per TMEM lane
-// quadrant for bf16 keys, one for fp8), then 8 fp8->bf16 converter warps
-// (fp8) or 4 spare warps that only take part in the CTA-wide barriers (bf16:
-// ptxas 13.0 for aarch64 hosts crashes on this kernel without them).
+// Warp roles: 0 TMA, 1 MMA, then the epilogue warps (three per TMEM lane
+// quadrant, or one with the fp8 -> bf16 converter), then 8 converter warps
+// (fp8 keys with bf16 q) or 2 spare warps that write the -inf tail (ptxas 13.0
+// for aarch64 hosts crashes on this kernel when no warps follow the epilogue).
 template <bool CONV>
 struct Roles {
-  static constexpr int kEpiWarps = CONV ? 4 : 8;
+  static constexpr int kEpiWarps = CONV ? 4 : 12;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kConvWarps = CONV ? 8 : 4;
+  static constexpr int kConvWarps = CONV ? 8 : 2;
   static constexpr int kConvThreads = 32 * kConvWarps;
   static constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
 };
