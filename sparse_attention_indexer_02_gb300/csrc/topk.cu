@@ -86,17 +86,30 @@ __device__ __forceinline__ uint4 keys4(const float4 f) {
   return make_uint4(topk_key(f.x), topk_key(f.y), topk_key(f.z), topk_key(f.w));
 }
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Keys of one CTA's segment: columns [0, nc4) from the shared-memory cache
-// (keys once pass 1 has converted them), the rest from global memory.
+// (keys once pass 1 has converted them; read through 32-bit shared-window
+// addresses), the rest from global memory.
 struct Segment {
   const float* x;  // first column of the segment
   const uint32_t* cache;
+  uint32_t cache_s;  // shared-window address of cache
   int len, nc4;
   bool vec;  // 16-byte global loads are aligned
 
   // keys of columns c .. c+3 (c a multiple of 4); lanes past len hold 0
   __device__ __forceinline__ uint4 get4(int c) const {
-    if (c + 4 <= nc4) return *reinterpret_cast<const uint4*>(cache + c);
+    if (c + 4 <= nc4) return lds128(cache_s + 4u * (uint32_t)c);
     if (vec && c + 4 <= len) return keys4(__ldg(reinterpret_cast<const float4*>(x + c)));
     uint32_t v[4];
 #pragma unroll
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
   const float* x = a.logits + row * a.row_stride + s0;
   const int nc4 = min(len, a.cap) & ~3;
   const int nchunks = a.bulk ? (nc4 + kChunk - 1) / kChunk : 0;
-  const Segment seg{x, cache, len, nc4, (reinterpret_cast<uintptr_t>(x) & 15u) == 0};
+  const Segment seg{x, cache, ptx::smem_u32(cache), len, nc4, (reinterpret_cast<uintptr_t>(x) & 15u) == 0};
 
   for (int i = threadIdx.x; i < kBins; i += kT) hist[i] = 0;
   if (multi)
@@ -302,14 +315,23 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
             }
           }
         }
-        kk = keys4(*reinterpret_cast<const float4*>(cache + c));
-        *reinterpret_cast<uint4*>(cache + c) = kk;
+        const uint4 f = lds128(seg.cache_s + 4u * (uint32_t)c);
+        kk = keys4(make_float4(__uint_as_float(f.x), __uint_as_float(f.y), __uint_as_float(f.z),
+                               __uint_as_float(f.w)));
+        sts128(seg.cache_s + 4u * (uint32_t)c, kk);
       } else {
         kk = seg.get4(c);
       }
+      if (c + 4 <= len) {  // every group but the segment's last: no per-key test
+        atomicAdd(&hist[kk.x >> 21], 1u);
+        atomicAdd(&hist[kk.y >> 21], 1u);
+        atomicAdd(&hist[kk.z >> 21], 1u);
+        atomicAdd(&hist[kk.w >> 21], 1u);
+      } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (c + u < len) atomicAdd(&hist[lane_of(kk, u) >> 21], 1u);
+        for (int u = 0; u < 3; ++u)
+          if (c + u < len) atomicAdd(&hist[lane_of(kk, u) >> 21], 1u);
+      }
     }
   }
   __syncthreads();
@@ -341,15 +363,16 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
     for (int c0 = w0; c0 < w1; c0 += kSeg) {  // warp-uniform trip count: collectives inside
       const int c = c0 + 4 * lane;
       const uint4 kk = seg.get4(c);
+      const int lim = w1 - c;  // keys of this lane's group inside the warp's range
       bool cnd[4];
       int nc = 0;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint32_t key = lane_of(kk, u);
-        const bool in = c + u < w1;
-        gt0 += in && (key >> 21) > d0;
-        cnd[u] = in && (key >> 21) == d0;
-        nc += cnd[u];
+        const uint32_t top = lane_of(kk, u) >> 21;
+        const bool in = u < lim;
+        gt0 += (int)(in & (top > d0));
+        cnd[u] = in & (top == d0);
+        nc += (int)cnd[u];
       }
       if (__any_sync(0xFFFFFFFFu, nc > 0)) {
         int incl = nc;
@@ -510,9 +533,10 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
     for (int c0 = w0; c0 < w1 && run < mine; c0 += kSeg) {  // warp-uniform
       const int c = c0 + 4 * lane;
       const uint4 kk = seg.get4(c);
+      const int lim = w1 - c;
       bool ge[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) ge[u] = c + u < w1 && lane_of(kk, u) >= thr;
+      for (int u = 0; u < 4; ++u) ge[u] = (u < lim) & (lane_of(kk, u) >= thr);
       if (!__any_sync(0xFFFFFFFFu, ge[0] | ge[1] | ge[2] | ge[3])) continue;
       bool sel[4];
       if (take_all_equal) {
