@@ -261,15 +261,16 @@ RAGGED = [
 
 
 @pytest.mark.parametrize("variant", list(VARIANTS))
-@pytest.mark.parametrize("kv_dtype", [qi.KV_BF16, qi.KV_FP8], ids=["bf16", "fp8"])
+@pytest.mark.parametrize("kv_dtype,q_dtype", [(qi.KV_BF16, qi.Q_BF16), (qi.KV_FP8, qi.Q_BF16),
+                                             (qi.KV_FP8, qi.Q_FP8)], ids=["bf16", "fp8", "fp8q"])
 @pytest.mark.parametrize("case", RAGGED, ids=[c[0] for c in RAGGED])
-def test_ragged_rows_match_oracle(oracle_mod, case, kv_dtype, variant):
+def test_ragged_rows_match_oracle(oracle_mod, case, kv_dtype, q_dtype, variant):
     name, B, rpr, H, pc, vis, oc, nn = case
     if kv_dtype == qi.KV_FP8 and (pc * 132) % 16:
         pytest.skip("a block-flat fp8 page of this size is not 16-byte aligned")
     R = B * rpr
     spec = qi.custom(name, B, rpr, H, pc, (vis * R)[:R], oc, k=32, kv_dtype=kv_dtype, seed=77,
-                     next_n_lens=nn)
+                     next_n_lens=nn, q_dtype=q_dtype)
     inp = qi.build_inputs(spec)
     if not supported(inp, VARIANTS[variant]):
         pytest.skip(f"{variant} does not serve this shape")
@@ -295,6 +296,33 @@ def test_ragged_dead_row_inputs_change_nothing():
     d["weights"][dead] = float("nan")
     got, _, _ = gpu_logits(inp, dev=d)
     assert torch.equal(got.view(torch.int32), base.view(torch.int32))
+
+
+def test_fp8_q_graph_replay_with_new_q(oracle_mod):
+    spec = qi.custom("q8_graph", 2, 4, 32, 64, [300, 301, 302, 303] * 2, 320, kv_dtype=qi.KV_FP8, seed=19,
+                     q_dtype=qi.Q_FP8)
+    inp = qi.build_inputs(spec)
+    d = qi.device_tensors(inp)
+    out = torch.empty((spec.num_rows, spec.out_cols), dtype=torch.float32, device="cuda")
+
+    def call():
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
+                                   scale_offset=inp.scale_offset, out=out)
+
+    call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    rng = np.random.default_rng(4)
+    for _ in range(2):
+        inp.q = qi._e4m3_codes(rng.standard_normal(inp.q.shape, dtype=np.float32))
+        d["q"].copy_(torch.from_numpy(inp.q).view(torch.float8_e4m3fn))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_logits_match(out.cpu().numpy(), oracle_mod.paged_mqa_logits(inp), qi.KV_FP8, where="q8 graph")
 
 
 def test_ragged_counts_rewritten_between_graph_replays(oracle_mod):
