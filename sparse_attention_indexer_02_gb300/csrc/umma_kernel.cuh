@@ -106,7 +106,7 @@ inline Layout make_layout(int N, int groups, int kind) {
   L.stage_bytes = fp8 ? kFp8StageAlloc : kTileBytes;
   L.a_stages = conv ? kFp8ConvStages : 0;
   const int ring = conv ? kScaleRing * kBM * 4 : 0;
-  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 +
+  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
                    8 * (groups + 1);
   int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;
@@ -117,7 +117,7 @@ inline Layout make_layout(int N, int groups, int kind) {
   const int nbars = 2 * L.stages + 2 * L.a_stages + (conv ? kScaleRing : 0) + 2 + 2 + 4;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
-  L.sched_off = L.epi_off + 2 * 256 * 4;        // pref[G + 1], gmax[G]
+  L.sched_off = L.epi_off + 2 * 256 * 4 + 16;   // pref[G + 1], gmax[G]
   L.total = 1024 + L.sched_off + 8 * (groups + 1);
   return L;
 }
@@ -577,6 +577,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     const int half = (warp - 2) >> 2;          // which of the quadrant's warps
     const int m = quad * 32 + lane;            // key row of the tile = TMEM lane
     const int64_t oc = p.out_cols;
+    const bool stream_out = p.stream_out != 0;
+    int32_t* const vis_min_s = vis_s + 256;  // smallest visible count of the group's rows
 
     // (1) computed tiles.  Column n of the accumulator is (row n / H, head
     // n % H).  A "unit" is the smallest run of 16-column TMEM loads that holds
@@ -598,13 +600,21 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         const int jj = g % p.groups_per_req;
         r0 = b * p.rows_per_req + jj * p.group_rows;
         nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+        if (et == 0) *vis_min_s = INT32_MAX;
         for (int i = et; i < nr * H; i += kEpiThreads) w_s[i] = p.weights[(int64_t)r0 * H + i];
-        for (int i = et; i < nr; i += kEpiThreads)
-          vis_s[i] = (int32_t)row_visible(p.visible, p.next_n_lens, r0 + i, p.rows_per_req, p.capacity);
+        epi_bar(kEpiThreads);
+        for (int i = et; i < nr; i += kEpiThreads) {
+          const int32_t v = (int32_t)row_visible(p.visible, p.next_n_lens, r0 + i, p.rows_per_req, p.capacity);
+          vis_s[i] = v;
+          atomicMin(vis_min_s, v);
+        }
         epi_bar(kEpiThreads);
         eg = g;
       }
-      const int64_t c = (int64_t)(t - pref[g]) * kBM + m;
+      const int tile_c0 = (t - pref[g]) * kBM;  // first column of the tile
+      const int64_t c = (int64_t)tile_c0 + m;
+      // every row of the group sees the whole tile: no mask, no bounds test
+      const bool unmasked = (int64_t)tile_c0 + kBM <= min((int64_t)*vis_min_s, oc);
       // fp8: this key's dequantisation scale.  relu(s x) = |s| relu(sign(s) x)
       // for every s, so the sign goes inside the ReLU and |s| is applied once
       // per row after the head sum.
@@ -668,10 +678,14 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
               part = fmaf(wh, relu_nan(xv), part);
             }
             if (FP8) part *= mag;
-            if (c < oc) {
+            float* const dst = ob + (int64_t)j * oc;
+            if (unmasked) {
+              if (stream_out) __stcs(dst, part + 0.0f);
+              else *dst = part + 0.0f;
+            } else if (c < oc) {
               const float val = c < vis_s[j] ? part + 0.0f : -INFINITY;
-              if (p.stream_out) __stcs(ob + (int64_t)j * oc, val);
-              else ob[(int64_t)j * oc] = val;
+              if (stream_out) __stcs(dst, val);
+              else *dst = val;
             }
           }
         }
