@@ -373,6 +373,17 @@ def run_gpu(args):
     def topk(d):  # ragged call: the top-k reads the live rows' visible counts
         torch_api.select_topk(d["out"], d.get("visible_live", d["visible"]), k, out=d["idx"])
 
+    # the same step as one qsa_paged_mqa_topk call; the host bound of the
+    # visible counts steers its dispatch (the selection inside the scoring
+    # kernel for decode-sized calls)
+    max_visible = int(spec.live_visible().max()) if R else 0
+
+    def fused(d):
+        torch_api.paged_mqa_topk(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"], k,
+                                 page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
+                                 scale_offset=inp.scale_offset, max_visible=max_visible, out_logits=d["out"],
+                                 out_idx=d["idx"], next_n_lens=d.get("next_n_lens"))
+
     # eager warm-up (first calls set kernel attributes), then CUDA graphs: the
     # host enqueues one graph per >= 16 steps, so launch overhead on the host
     # never shows up in the device timings.
@@ -441,6 +452,17 @@ def run_gpu(args):
     score_us = time_graph(g_score, per_graph, reps)
     topk_us = time_graph(g_topk, per_graph, reps)
     del g_step, g_rem, g_score, g_topk
+    # the one-call form (eager first: its workspace is allocated outside capture)
+    for i in range(3):
+        fused(sets[i % copies])
+    fused_variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
+    torch.cuda.synchronize(dev)
+    g_fused = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fused):
+        for i in range(per_graph):
+            fused(sets[i % copies])
+    fused_us = time_graph(g_fused, per_graph, reps)
+    del g_fused
 
     max_ms = max_over_ranks(total_ms)
     ms_step = max_ms / K
@@ -508,6 +530,7 @@ def run_gpu(args):
             "us_per_call": round(score_us, 3), "key_gbs_scoring": round(key_bytes / (score_us * 1e-6) / 1e9, 1),
             "topk_us_per_row": round(topk_us / R, 4), "topk_us_per_call": round(topk_us, 3),
             "step_us": round(1e3 * ms_step, 3),
+            "fused_step_us": round(fused_us, 3), "fused_variant": fused_variant,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 2 * K, "clocks": clocks,
         }

@@ -34,6 +34,7 @@
 #ifndef QSA_H_
 #define QSA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -59,7 +60,9 @@ typedef enum qsa_kv_dtype {
 typedef enum qsa_variant {
   QSA_VARIANT_AUTO = -1,
   QSA_VARIANT_ROWCORE = 0, /* CUDA-core scorer, one row at a time; any shape */
-  QSA_VARIANT_UMMA = 1     /* tcgen05 scorer: 128 keys in M, a request's rows x heads in N */
+  QSA_VARIANT_UMMA = 1,    /* tcgen05 scorer: 128 keys in M, a request's rows x heads in N */
+  QSA_VARIANT_UMMA_TOPK = 2 /* tcgen05 scorer with the selection in the same kernel
+                               (qsa_paged_mqa_topk; reported by qsa_last_variant only) */
 } qsa_variant;
 
 /* Shape of one qsa_paged_mqa_logits call.  All sizes are host values. */
@@ -178,6 +181,51 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
                            void* stream);
 
 /*
+ * qsa_paged_mqa_topk - qsa_paged_mqa_logits_ex and then the top-k of every row,
+ * in one call (one kernel for decode-sized calls).
+ *
+ * The pages score and then select in two steps, and vLLM #62589 "Details"
+ * notes that the only consumer of the logits, the decode top-k, reads each
+ * row's [0, visible) alone; here the selection of a row starts in the scoring
+ * kernel as soon as every tile of the row is stored, with the logits still in
+ * L2, instead of after a second launch.
+ *
+ * Results: out_logits exactly as qsa_paged_mqa_logits_ex writes them; out_idx
+ * exactly as qsa_select_topk(out_logits, R, out_cols, n, k, out_idx) writes
+ * it, where n[r] is the row's scored visible count: visible_cols[r] clamped
+ * to [0, min(out_cols, max_pages * page_cols)], and 0 for a dead row of the
+ * ragged call (so a dead row selects nothing: k slots of -1).
+ *
+ * Arguments: as qsa_paged_mqa_logits_ex, plus
+ *   k            1..2048 selected columns per row.
+ *   max_visible  host value: the caller's bound on the visible counts, or 0
+ *                (unknown; out_cols and the page capacity bound them).  Like
+ *                vLLM #62589's single_row_decode flag it only steers the
+ *                dispatch: the selection runs in the scoring kernel for at
+ *                most 256 rows whose bound is at most 16384 columns, and as a
+ *                separate top-k launch (which splits long rows over a thread-
+ *                block cluster) otherwise.  A wrong bound costs speed only.
+ *   out_idx      int32 [R][k] (device), 4-byte aligned.
+ *   workspace    device memory of at least qsa_paged_mqa_topk_workspace(desc)
+ *                bytes, 4-byte aligned (NULL when that size is 0).  It must
+ *                hold zeros before the first call; every completed call leaves
+ *                it zero again.  Calls that may run at the same time (other
+ *                streams) need their own workspaces.
+ * Errors as qsa_paged_mqa_logits_ex; k out of range, a NULL or misaligned
+ * out_idx, or a missing or short workspace: QSA_ERR_INVALID_ARG.
+ */
+qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* desc, int32_t q_dtype, const void* q, const float* weights,
+                              const void* kv_cache, const float* scales, const int32_t* block_table,
+                              const int32_t* visible_cols, const int32_t* next_n_lens, int32_t k,
+                              int64_t max_visible, float* out_logits, int32_t* out_idx, void* workspace,
+                              size_t workspace_bytes, void* stream);
+
+/* Workspace bytes qsa_paged_mqa_topk needs for `desc` (host only; 0 when the
+ * shape never runs the fused selection): 4 * (2 * G + 1) for the G <= 256 row
+ * groups of the tcgen05 scorer. */
+qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* bytes);
+
+/*
  * qsa_plan_variant - host-only dispatch decision for `desc` (no CUDA call).
  * Writes the qsa_variant qsa_paged_mqa_logits would launch (honouring
  * qsa_force_variant) to *variant.  The choice uses host metadata only, with no
@@ -195,7 +243,8 @@ qsa_status qsa_plan_variant(const qsa_paged_desc* desc, int32_t* variant);
  * QSA_ERR_UNSUPPORTED.  Meant for tests and A/B measurements. */
 void qsa_force_variant(int32_t variant);
 
-/* Variant launched by this thread's last successful qsa_paged_mqa_logits. */
+/* Variant launched by this thread's last successful scoring call
+ * (qsa_paged_mqa_logits and its _ragged / _ex forms, qsa_paged_mqa_topk). */
 int32_t qsa_last_variant(void);
 
 /* Static description of a status code, and of this thread's last failure. */

@@ -17,11 +17,12 @@ LIB_PATH = os.path.join(_PKG, "libqsa.so")
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 KV_BF16, KV_FP8_E4M3 = 0, 1
 Q_BF16, Q_FP8_E4M3 = 0, 1
-VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA = -1, 0, 1
-VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma"}
+VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA, VARIANT_UMMA_TOPK = -1, 0, 1, 2
+VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma", VARIANT_UMMA_TOPK: "umma+topk"}
 
 # Every symbol include/qsa.h declares.
-EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_paged_mqa_topk",
+            "qsa_paged_mqa_topk_workspace", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
@@ -63,6 +64,11 @@ def load_library():
         lib.qsa_paged_mqa_logits_ragged.argtypes = [ctypes.POINTER(PagedDesc), vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.qsa_paged_mqa_logits_ex.restype = ctypes.c_int
         lib.qsa_paged_mqa_logits_ex.argtypes = [ctypes.POINTER(PagedDesc), i32, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.qsa_paged_mqa_topk.restype = ctypes.c_int
+        lib.qsa_paged_mqa_topk.argtypes = [ctypes.POINTER(PagedDesc), i32, vp, vp, vp, vp, vp, vp, vp, i32, i64, vp,
+                                           vp, vp, ctypes.c_size_t, vp]
+        lib.qsa_paged_mqa_topk_workspace.restype = ctypes.c_int
+        lib.qsa_paged_mqa_topk_workspace.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(ctypes.c_size_t)]
         lib.qsa_select_topk.restype = ctypes.c_int
         lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         lib.qsa_plan_variant.restype = ctypes.c_int
@@ -138,6 +144,25 @@ def paged_mqa_logits(desc: PagedDesc, q, weights, kv_cache, scales, block_table,
                                              _addr(scales), _addr(block_table), _addr(visible_cols),
                                              _addr(next_n_lens), _addr(out_logits), _stream(stream))
     _check(st)
+
+
+def paged_mqa_topk(desc: PagedDesc, q, weights, kv_cache, scales, block_table, visible_cols, k: int,
+                   out_logits, out_idx, workspace, workspace_bytes: int, stream=None, next_n_lens=None,
+                   q_dtype: int = Q_BF16, max_visible: int = 0) -> None:
+    """qsa_paged_mqa_topk: scoring and the per-row top-k in one call."""
+    st = load_library().qsa_paged_mqa_topk(ctypes.byref(desc), int(q_dtype), _addr(q), _addr(weights),
+                                           _addr(kv_cache), _addr(scales), _addr(block_table),
+                                           _addr(visible_cols), _addr(next_n_lens), int(k), int(max_visible),
+                                           _addr(out_logits), _addr(out_idx), _addr(workspace),
+                                           int(workspace_bytes), _stream(stream))
+    _check(st)
+
+
+def topk_workspace_bytes(desc: PagedDesc) -> int:
+    """Workspace bytes paged_mqa_topk needs for this shape (zeroed before first use)."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().qsa_paged_mqa_topk_workspace(ctypes.byref(desc), ctypes.byref(n)))
+    return n.value
 
 
 def select_topk(logits, num_rows: int, row_stride: int, visible_cols, k: int, out_idx, stream=None) -> None:

@@ -142,10 +142,16 @@ qsa_status qsa_paged_mqa_logits_ragged(const qsa_paged_desc* d, const void* q, c
                                  next_n_lens, out_logits, stream);
 }
 
-qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* d, int32_t q_dtype, const void* q,
-                                   const float* weights, const void* kv_cache, const float* scales,
-                                   const int32_t* block_table, const int32_t* visible_cols,
-                                   const int32_t* next_n_lens, float* out_logits, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation, variant choice and launch parameters shared by the scoring
+// calls.  Returns QSA_OK with *empty set when there is nothing to compute.
+qsa_status prepare_scoring(const qsa_paged_desc* d, int32_t q_dtype, const void* q, const float* weights,
+                           const void* kv_cache, const float* scales, const int32_t* block_table,
+                           const int32_t* visible_cols, const int32_t* next_n_lens, float* out_logits,
+                           qsa::ScoreParams* p, int32_t* variant, bool* empty) {
   qsa_status st = validate_desc(d);
   if (st != QSA_OK) return st;
   const int64_t rows = (int64_t)d->num_requests * d->rows_per_req;
@@ -156,10 +162,8 @@ qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* d, int32_t q_dtype, con
   if (q8 && !fp8) return fail(QSA_ERR_INVALID_ARG, "fp8 q needs fp8 keys (mixed operand types)");
   if (fp8 && !scales) return fail(QSA_ERR_INVALID_ARG, "fp8 keys need a scales pointer");
   if (!fp8 && scales) return fail(QSA_ERR_INVALID_ARG, "bf16 keys take no scales (mixed operand types)");
-  if (rows == 0 || d->out_cols == 0) {
-    g_last_variant = -1;
-    return QSA_OK;
-  }
+  *empty = rows == 0 || d->out_cols == 0;
+  if (*empty) return QSA_OK;
   if (!q || !weights || !kv_cache || !block_table || !visible_cols || !out_logits)
     return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(q, 16) || !aligned(kv_cache, 16))
@@ -168,49 +172,137 @@ qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* d, int32_t q_dtype, con
       !aligned(out_logits, 4) || (fp8 && !aligned(scales, 4)) || !aligned(next_n_lens, 4))
     return fail(QSA_ERR_INVALID_ARG,
                 "weights, block_table, visible_cols, next_n_lens, out_logits, scales must be 4-byte aligned");
-  int32_t variant = 0;
-  st = qsa_plan_variant(d, &variant);
+  st = qsa_plan_variant(d, variant);
   if (st != QSA_OK) return st;
   // the tcgen05 scorer bulk-copies fp8 scales, which needs a 16-byte aligned base
-  if (variant == QSA_VARIANT_UMMA && fp8 && !aligned(scales, 16)) {
+  if (*variant == QSA_VARIANT_UMMA && fp8 && !aligned(scales, 16)) {
     if (g_forced_variant.load() == QSA_VARIANT_UMMA)
       return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant needs 16-byte aligned fp8 scales");
-    variant = QSA_VARIANT_ROWCORE;
+    *variant = QSA_VARIANT_ROWCORE;
   }
-
-  qsa::ScoreParams p;
-  p.q = static_cast<const uint16_t*>(q);
-  p.weights = weights;
-  p.kv = static_cast<const uint8_t*>(kv_cache);
-  p.scales = reinterpret_cast<const uint8_t*>(scales);
-  p.block_table = block_table;
-  p.visible = visible_cols;
-  p.next_n_lens = next_n_lens;
-  p.out = out_logits;
-  p.out_cols = d->out_cols;
-  p.key_page_stride = d->key_page_stride;
-  p.scale_page_stride = fp8 ? d->scale_page_stride : 0;
+  p->q = static_cast<const uint16_t*>(q);
+  p->weights = weights;
+  p->kv = static_cast<const uint8_t*>(kv_cache);
+  p->scales = reinterpret_cast<const uint8_t*>(scales);
+  p->block_table = block_table;
+  p->visible = visible_cols;
+  p->next_n_lens = next_n_lens;
+  p->out = out_logits;
+  p->out_cols = d->out_cols;
+  p->key_page_stride = d->key_page_stride;
+  p->scale_page_stride = fp8 ? d->scale_page_stride : 0;
   const int64_t cap = (int64_t)d->max_pages * d->page_cols;
-  p.capacity = cap < d->out_cols ? cap : d->out_cols;
-  p.num_requests = d->num_requests;
-  p.rows_per_req = d->rows_per_req;
-  p.num_rows = (int32_t)rows;
-  p.num_heads = d->num_heads;
-  p.page_cols = d->page_cols;
-  p.max_pages = d->max_pages;
-  p.num_pages = d->num_pages;
-  p.fp8 = fp8 ? 1 : 0;
-  p.q8 = q8 ? 1 : 0;
+  p->capacity = cap < d->out_cols ? cap : d->out_cols;
+  p->num_requests = d->num_requests;
+  p->rows_per_req = d->rows_per_req;
+  p->num_rows = (int32_t)rows;
+  p->num_heads = d->num_heads;
+  p->page_cols = d->page_cols;
+  p->max_pages = d->max_pages;
+  p->num_pages = d->num_pages;
+  p->fp8 = fp8 ? 1 : 0;
+  p->q8 = q8 ? 1 : 0;
+  return QSA_OK;
+}
 
+qsa_status launch_scoring(const qsa::ScoreParams& p, int32_t variant, cudaStream_t s,
+                          const qsa::FuseArgs* fuse) {
   const char* msg = "launch failed";
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = variant == QSA_VARIANT_UMMA ? qsa::launch_umma(p, s, &msg)
+  cudaError_t e = variant == QSA_VARIANT_UMMA ? qsa::launch_umma(p, s, &msg, fuse)
                                               : qsa::launch_rowcore(p, s, &msg);
   if (e == cudaErrorInvalidValue && msg && strcmp(msg, "launch failed") != 0)
     return fail(QSA_ERR_UNSUPPORTED, "%s", msg);
   if (e != cudaSuccess)
     return fail(QSA_ERR_CUDA, "scoring launch (variant %d): %s", variant, cudaGetErrorString(e));
   g_last_variant = variant;
+  return QSA_OK;
+}
+
+// The fused selection is used for decode-sized calls: at most kFuseMaxRows
+// rows, none longer than kFuseMaxVisible columns (up to there one CTA a row is
+// as fast as any split of the row, the top-k kernel's own rule; longer rows go
+// to the cluster split of the separate top-k launch).
+constexpr int64_t kFuseMaxRows = 256;
+constexpr int64_t kFuseMaxVisible = 16384;
+
+// Workspace words of the fused selection for `d` (0: the shape is never fused).
+int64_t fused_words(const qsa_paged_desc* d) {
+  const char* why = nullptr;
+  if (!qsa::umma_supports(*d, &why)) return 0;
+  const int64_t G = qsa::umma_num_groups(*d);
+  return G >= 1 && G <= qsa::kFuseMaxGroups ? 2 * G + 1 : 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* d, int32_t q_dtype, const void* q,
+                                   const float* weights, const void* kv_cache, const float* scales,
+                                   const int32_t* block_table, const int32_t* visible_cols,
+                                   const int32_t* next_n_lens, float* out_logits, void* stream) {
+  qsa::ScoreParams p;
+  int32_t variant = 0;
+  bool empty = false;
+  qsa_status st = prepare_scoring(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols,
+                                  next_n_lens, out_logits, &p, &variant, &empty);
+  if (st != QSA_OK) return st;
+  if (empty) {
+    g_last_variant = -1;
+    return QSA_OK;
+  }
+  return launch_scoring(p, variant, static_cast<cudaStream_t>(stream), nullptr);
+}
+
+qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* d, size_t* bytes) {
+  qsa_status st = validate_desc(d);
+  if (st != QSA_OK) return st;
+  if (!bytes) return fail(QSA_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = (size_t)fused_words(d) * 4;
+  return QSA_OK;
+}
+
+qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* d, int32_t q_dtype, const void* q, const float* weights,
+                              const void* kv_cache, const float* scales, const int32_t* block_table,
+                              const int32_t* visible_cols, const int32_t* next_n_lens, int32_t k,
+                              int64_t max_visible, float* out_logits, int32_t* out_idx, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  qsa::ScoreParams p;
+  int32_t variant = 0;
+  bool empty = false;
+  qsa_status st = prepare_scoring(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols,
+                                  next_n_lens, out_logits, &p, &variant, &empty);
+  if (st != QSA_OK) return st;
+  if (k < 1 || k > 2048) return fail(QSA_ERR_INVALID_ARG, "k must be in 1..2048 (got %d)", k);
+  if (empty) {
+    g_last_variant = -1;
+    if ((int64_t)d->num_requests * d->rows_per_req == 0) return QSA_OK;
+    // rows but no column: every row selects nothing
+    if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be 4-byte aligned");
+    const size_t n = (size_t)d->num_requests * d->rows_per_req * k * sizeof(int32_t);
+    cudaError_t e = cudaMemsetAsync(out_idx, 0xFF, n, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "filling out_idx: %s", cudaGetErrorString(e));
+    return QSA_OK;
+  }
+  if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be non-NULL, 4-byte aligned");
+  const int64_t words = fused_words(d);
+  if (words > 0 && (!workspace || !aligned(workspace, 4) || workspace_bytes < (size_t)words * 4))
+    return fail(QSA_ERR_INVALID_ARG, "workspace must be 4-byte aligned and hold %lld bytes", (long long)words * 4);
+  const int64_t bound = max_visible > 0 && max_visible < p.capacity ? max_visible : p.capacity;
+  const bool fused =
+      variant == QSA_VARIANT_UMMA && words > 0 && p.num_rows <= kFuseMaxRows && bound <= kFuseMaxVisible;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fused) {
+    const qsa::FuseArgs fa{out_idx, static_cast<uint32_t*>(workspace), k};
+    st = launch_scoring(p, variant, s, &fa);
+    if (st == QSA_OK) g_last_variant = QSA_VARIANT_UMMA_TOPK;
+    return st;
+  }
+  st = launch_scoring(p, variant, s, nullptr);
+  if (st != QSA_OK) return st;
+  cudaError_t e = qsa::launch_topk(out_logits, p.num_rows, p.out_cols, visible_cols, next_n_lens, p.rows_per_req,
+                                   p.capacity, k, out_idx, s);
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
 }
 
@@ -231,8 +323,8 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
   if (!logits || !visible_cols || !out_idx) return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(logits, 4) || !aligned(visible_cols, 4) || !aligned(out_idx, 4))
     return fail(QSA_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
-  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, k, out_idx,
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, nullptr, 1, row_stride, k,
+                                   out_idx, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
 }

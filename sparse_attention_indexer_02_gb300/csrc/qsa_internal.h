@@ -27,19 +27,34 @@ struct ScoreParams {
   int32_t q8;               // q as e4m3 codes [R][H][128] (fp8 keys only)
 };
 
+// Selection fused into a tcgen05 scoring launch (qsa_paged_mqa_topk).
+constexpr int kFuseMaxGroups = 256;  // row groups a fused launch takes at most
+struct FuseArgs {
+  int32_t* topk_out;  // [num_rows][k]
+  uint32_t* sync;     // 2 * groups + 1 words, zero (and zero again once the launch completes)
+  int32_t k;
+};
+
 // Each launcher returns cudaSuccess or the launch error; `msg` gets a reason
 // when a shape is rejected (then the return is cudaErrorInvalidValue).
 cudaError_t launch_rowcore(const ScoreParams& p, cudaStream_t stream, const char** msg);
 bool umma_supports(const qsa_paged_desc& d, const char** why);
-cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg);
+// Row groups the tcgen05 scorer splits `d` into (rows x heads of a group <= 256).
+int64_t umma_num_groups(const qsa_paged_desc& d);
+cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg,
+                        const FuseArgs* fuse = nullptr);
 // Device address of the fault word on the current device (bit 0: a scoring
 // kernel's bounded wait gave up; bit 1: a top-k kernel's).
 cudaError_t fault_word_address(unsigned int** out);
 // Reads (and optionally clears) the device fault word the kernels set when a
 // bounded wait gives up.  Synchronises the device.
 cudaError_t read_fault_word(uint32_t* flags, bool clear);
-cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride,
-                        const int32_t* visible, int32_t k, int32_t* out, cudaStream_t stream);
+// Top-k of every row over [0, n_r): n_r = visible[r] clamped to [0, min(capacity,
+// row_stride)], and 0 for a dead row (next_n_lens non-null: row r is dead when
+// r % rows_per_req >= next_n_lens[r / rows_per_req]).
+cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
+                        const int32_t* next_n_lens, int32_t rows_per_req, int64_t capacity, int32_t k,
+                        int32_t* out, cudaStream_t stream);
 
 // Cached per-device properties (queried once per device).
 struct DeviceInfo {

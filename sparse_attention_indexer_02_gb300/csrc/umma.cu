@@ -112,7 +112,13 @@ bool umma_supports(const qsa_paged_desc& d, const char** why) {
   return true;
 }
 
-cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg) {
+int64_t umma_num_groups(const qsa_paged_desc& d) {
+  int Gr, N;
+  group_shape(d, &Gr, &N);
+  return (int64_t)d.num_requests * ((d.rows_per_req + Gr - 1) / Gr);
+}
+
+cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg, const FuseArgs* fuse) {
   if (p.num_rows == 0 || p.out_cols == 0) return cudaSuccess;
   qsa_paged_desc d{};
   d.num_requests = p.num_requests;
@@ -202,7 +208,35 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   const int64_t upper = (int64_t)up.num_groups * up.tiles_cap;
   const int grid = (int)(upper < info.num_sms ? (upper < 1 ? 1 : upper) : info.num_sms);
   const int kind = !p.fp8 ? kKindBf16 : (p.q8 ? kKindFp8Q : kKindFp8Keys);
-  const Layout L = make_layout(N, up.num_groups, kind);
+  const Layout L = make_layout(N, up.num_groups, kind, fuse != nullptr);
+  up.topk_out = nullptr;
+  up.fuse_sync = nullptr;
+  up.topk_k = up.topk_cap = up.topk_cpw = 0;
+  if (fuse) {
+    if (up.num_groups > kFuseMaxGroups) {
+      *msg = "too many row groups for the fused selection";
+      return cudaErrorInvalidValue;
+    }
+    // the selection runs on 512 threads (256 with the converter warps) in the
+    // stage area, idle once the CTA's tiles are scored: per-warp candidate
+    // lists, the histogram and as much of a row as fits cached
+    const int nt = kind == kKindFp8Keys ? 256 : 512;
+    const int cpw = sel::kCpwMax;
+    const int64_t room = ((int64_t)L.bar_off - kSelSharedBytes) / 4 - (int64_t)(nt / 32) * cpw - sel::kBins;
+    const int64_t cap = (room < sel::kCacheMax ? room : sel::kCacheMax) & ~int64_t(3);
+    if (cap < 4) {
+      *msg = "no shared memory left for the fused selection";
+      return cudaErrorInvalidValue;
+    }
+    up.topk_out = fuse->topk_out;
+    up.fuse_sync = fuse->sync;
+    up.topk_k = fuse->k;
+    up.topk_cap = (int32_t)cap;
+    up.topk_cpw = cpw;
+    if (kind == kKindFp8Q) return launch_q8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);
+    return p.fp8 ? launch_fp8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream)
+                 : launch_bf16_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);
+  }
   if (kind == kKindFp8Q) return launch_q8(p.num_heads, kv_map, q_map, up, L, grid, stream);
   return p.fp8 ? launch_fp8(p.num_heads, kv_map, q_map, up, L, grid, stream)
                : launch_bf16(p.num_heads, kv_map, q_map, up, L, grid, stream);

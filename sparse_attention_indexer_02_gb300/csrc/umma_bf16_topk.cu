@@ -1,0 +1,13 @@
+// tcgen05 scorer with the fused per-row selection, bf16 keys (see umma_kernel.cuh).
+#include "umma_kernel.cuh"
+
+namespace qsa {
+namespace umma {
+
+cudaError_t launch_bf16_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                             const Layout& L, int grid, cudaStream_t s) {
+  return launch_any<kKindBf16, true>(heads, kv, qm, up, L, grid, s);
+}
+
+}  // namespace umma
+}  // namespace qsa

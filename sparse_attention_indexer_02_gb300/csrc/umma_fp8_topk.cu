@@ -1,0 +1,13 @@
+// tcgen05 scorer with the fused per-row selection, fp8 keys widened for bf16 q (see umma_kernel.cuh).
+#include "umma_kernel.cuh"
+
+namespace qsa {
+namespace umma {
+
+cudaError_t launch_fp8_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                            const Layout& L, int grid, cudaStream_t s) {
+  return launch_any<kKindFp8Keys, true>(heads, kv, qm, up, L, grid, s);
+}
+
+}  // namespace umma
+}  // namespace qsa

@@ -35,6 +35,7 @@
 #include "device_common.cuh"
 #include "qsa_internal.h"
 #include "sm100_ptx.cuh"
+#include "topk_select.cuh"
 
 namespace qsa {
 namespace umma {
@@ -64,6 +65,12 @@ struct Roles {
 constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kFastSchedRows = 256;              // up to this many rows one warp builds the schedule
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in limit per CTA
+// Fused selection: at most kFuseMaxGroups row groups (their counters live in
+// the caller's workspace, the list of groups a CTA completed in shared memory).
+constexpr int kFuseWords = 4 + kFuseMaxGroups;   // won count, claim key, claimed row, last flag; won groups
+constexpr int kSelSharedBytes = 512;             // sel::Shared at the start of the stage area
+constexpr int kFuseKeys = 16;                    // keys per thread of the register selection path
+static_assert(sizeof(sel::Shared) <= kSelSharedBytes, "selection state must fit its slot");
 
 
 struct UmmaParams {
@@ -83,6 +90,10 @@ struct UmmaParams {
   int32_t pc_shift;   // log2(page_cols) when page_cols is a power of two, else -1
   int32_t stream_out;  // logits far larger than L2: write them with evict-first stores
   int32_t keep_keys;   // several row groups reuse each key tile: keep keys in L2
+  // fused selection (kernels instantiated with FUSE only)
+  int32_t* topk_out;    // [num_rows][topk_k] selected columns
+  uint32_t* fuse_sync;  // caller workspace: done[G] | cursor[G] | finished; zero between calls
+  int32_t topk_k, topk_cap, topk_cpw;
 };
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-aligned base);
@@ -94,10 +105,10 @@ struct Layout {
   int32_t a_stages;     // fp8: bf16 operand stages written by the converter; bf16: 0
   int32_t tmem_cols;    // 2 accumulators of N columns, power of two >= 32
   uint32_t idesc;       // tcgen05 instruction descriptor for M = 128, this N
-  int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, total;
+  int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, fuse_off, total;
 };
 
-inline Layout make_layout(int N, int groups, int kind) {
+inline Layout make_layout(int N, int groups, int kind, bool fused = false) {
   const bool fp8 = kind != kKindBf16, conv = kind == kKindFp8Keys;
   Layout L;
   L.n = N;
@@ -107,7 +118,7 @@ inline Layout make_layout(int N, int groups, int kind) {
   L.a_stages = conv ? kFp8ConvStages : 0;
   const int ring = conv ? kScaleRing * kBM * 4 : 0;
   const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
-                   8 * (groups + 1);
+                   8 * (groups + 1) + (fused ? 16 + 4 * kFuseWords : 0);
   int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;
   L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
@@ -118,7 +129,8 @@ inline Layout make_layout(int N, int groups, int kind) {
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4 + 16;   // pref[G + 1], gmax[G]
-  L.total = 1024 + L.sched_off + 8 * (groups + 1);
+  L.fuse_off = (L.sched_off + 8 * (groups + 1) + 15) & ~15;  // fused: kFuseWords ints
+  L.total = 1024 + (fused ? L.fuse_off + 4 * kFuseWords : L.sched_off + 8 * (groups + 1));
   return L;
 }
 
@@ -234,7 +246,137 @@ __device__ __forceinline__ void fill_tail(const UmmaParams& p, const int32_t* pr
   }
 }
 
-template <int H, int KIND>
+// ---- fused selection -------------------------------------------------------
+// Every CTA counts, per row group, the tiles whose logits it has stored
+// (done[g], a release); the CTA whose count completes a group (an acquire)
+// has every logit of the group's rows behind it and selects them once its own
+// tiles are done.  Groups of one row: that is all, and the completing CTA
+// puts the count back to zero.  Groups of several rows: the completing CTA
+// selects row 0 and then takes rows from cursor[g]; the other CTAs that
+// scored the group wait for it to complete (a bounded wait: a CTA that gives
+// up leaves its rows to the others, never a row unselected) and take rows
+// too; the last CTA to finish zeroes the counters.  Groups without tiles (no
+// row sees a column) select nothing and need no logits.
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+constexpr long long kHelpSpinCycles = 200000;  // ~0.1 ms: a helper's wait for a group to complete
+
+// The epilogue has stored `run` tiles of group g: add them to the group's
+// count (one thread, after a barrier of the epilogue threads, so the count is
+// a release of all of their stores) and record the group when it completes.
+__device__ __forceinline__ void fuse_close(const UmmaParams& p, const int32_t* pref, int g, int run, int et,
+                                           int32_t* fz, int nthreads) {
+  epi_bar(nthreads);
+  if (et == 0) {
+    const uint32_t T = (uint32_t)(pref[g + 1] - pref[g]);
+    const uint32_t old = atom_add_acq_rel_gpu(p.fuse_sync + g, (uint32_t)run);
+    if (old + (uint32_t)run == T) fz[4 + fz[0]++] = g;
+  }
+}
+
+__device__ __forceinline__ int group_nrows(const UmmaParams& p, int g) {
+  const int jj = g % p.groups_per_req;
+  return min(p.group_rows, p.rows_per_req - jj * p.group_rows);
+}
+
+__device__ __forceinline__ int64_t group_row0(const UmmaParams& p, int g) {
+  const int b = g / p.groups_per_req, jj = g - b * p.groups_per_req;
+  return (int64_t)b * p.rows_per_req + (int64_t)jj * p.group_rows;
+}
+
+// Selection of the groups' rows by threads [0, NT) once the CTA's scoring is
+// done; the stage area (`smem`, L.bar_off bytes, idle by now) holds the
+// selection's shared memory.  [t_begin, t_end) are the CTA's tiles.
+template <int NT>
+__device__ __forceinline__ void fused_select(const UmmaParams& p, const int32_t* pref, int G, int t_begin,
+                                             int t_end, uint8_t* smem, int32_t* fz) {
+  const int tid = (int)threadIdx.x;
+  const int k = p.topk_k;
+  sel::Shared& sh = *reinterpret_cast<sel::Shared*>(smem);
+  uint32_t* dyn = reinterpret_cast<uint32_t*>(smem + kSelSharedBytes);
+  const sel::Config cf{k, p.topk_cap, p.topk_cpw, 0, p.fault};
+  uint32_t* done = p.fuse_sync;
+  uint32_t* cursor = done + G;
+  uint32_t* finished = done + 2 * G;
+  // shared memory the tensor core and the copies used is written by plain stores now
+  ptx::fence_proxy_async_smem();
+  auto select = [&](int g, int j) {  // row j of group g
+    const int64_t r = group_row0(p, g) + j;
+    const int n = (int)row_visible(p.visible, p.next_n_lens, r, p.rows_per_req, p.capacity);
+    const sel::RowTask task{p.out + r * p.out_cols, n, p.topk_out + r * k};
+    sel::select_row<NT, false, true, kFuseKeys>(task, cf, dyn, sh, 1, 0);
+    sel::bar_sync<NT>();
+  };
+  auto claim = [&](int g) -> int {  // next row of g nobody has taken (>= its row count: none)
+    if (tid == 0) fz[2] = 1 + (int)atomicAdd(cursor + g, 1u);
+    sel::bar_sync<NT>();
+    const int j = fz[2];
+    sel::bar_sync<NT>();
+    return j;
+  };
+
+  // (0) groups without tiles: every row selects nothing
+  for (int g = blockIdx.x; g < G; g += gridDim.x)
+    if (pref[g + 1] == pref[g]) {
+      int32_t* o = p.topk_out + group_row0(p, g) * k;
+      for (int i = tid; i < group_nrows(p, g) * k; i += NT) o[i] = -1;
+    }
+  const bool multi = p.group_rows > 1;
+  // (1) the groups this CTA completed
+  const int nwon = fz[0];
+  for (int w = 0; w < nwon; ++w) {
+    const int g = fz[4 + w];
+    if (!multi && tid == 0) done[g] = 0u;  // every count of the group is in: reset for the next call
+    select(g, 0);
+    const int nr = group_nrows(p, g);
+    if (nr > 1)
+      for (int j = claim(g); j < nr; j = claim(g)) select(g, j);
+  }
+  if (!multi) return;
+  // (2) rows of the other groups this CTA scored, once they complete
+  if (t_begin < t_end) {
+    const int g1 = find_group(pref, G, t_end - 1);
+    for (int g = find_group(pref, G, t_begin); g <= g1; ++g) {
+      bool mine = false;
+      for (int w = 0; w < nwon; ++w) mine |= fz[4 + w] == g;
+      if (mine || group_nrows(p, g) < 2) continue;
+      if (tid == 0) {
+        const uint32_t T = (uint32_t)(pref[g + 1] - pref[g]);
+        const long long t0 = clock64();
+        bool ok;
+        while (!(ok = ld_acquire_gpu(done + g) == T) && clock64() - t0 < kHelpSpinCycles) {
+        }
+        fz[1] = ok ? 1 : 0;
+      }
+      sel::bar_sync<NT>();
+      const bool ready = fz[1] != 0;
+      sel::bar_sync<NT>();
+      if (!ready) continue;
+      const int nr = group_nrows(p, g);
+      for (int j = claim(g); j < nr; j = claim(g)) select(g, j);
+    }
+  }
+  // (3) the last CTA out zeroes the counters
+  if (tid == 0) fz[3] = atom_add_acq_rel_gpu(finished, 1u) == gridDim.x - 1 ? 1 : 0;
+  sel::bar_sync<NT>();
+  if (fz[3]) {
+    for (int i = tid; i < 2 * G; i += NT) done[i] = 0u;
+    if (tid == 0) *finished = 0u;
+  }
+}
+
+template <int H, int KIND, bool FUSE>
 __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     umma_score_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const UmmaParams p, const Layout L) {
@@ -269,6 +411,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
   int32_t* vis_s = reinterpret_cast<int32_t*>(w_s + 256);
   int32_t* pref = reinterpret_cast<int32_t*>(smem + L.sched_off);
   int32_t* gmax = pref + p.num_groups + 1;
+  int32_t* fz = reinterpret_cast<int32_t*>(smem + L.fuse_off);  // FUSE: won groups and claim slots
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -301,6 +444,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     ptx::mbar_init(mma_done, 1);
     ptx::mbar_init(setup, 2);
     *abort_flag = 0;
+    if (FUSE) fz[0] = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&kv_map);
     ptx::prefetch_tmap(&q_map);
@@ -591,10 +735,15 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     uint32_t acc_phase = 0;
     int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
     int eg = -1, r0 = 0, nr = 0, b = 0;
+    int run = 0;  // FUSE: tiles of group eg stored in this CTA's current run
     bool ok = true;
-    for (int t = t_begin; t < t_end && ok; ++t) {
+    // After a failed wait a thread keeps walking the tiles without work, so
+    // every epilogue thread meets the same barriers at group changes.
+    for (int t = t_begin; t < t_end; ++t) {
       while (t >= pref[g + 1]) ++g;
       if (g != eg) {
+        if (FUSE && eg >= 0) fuse_close(p, pref, eg, run, et, fz, kEpiThreads);
+        run = 0;
         epi_bar(kEpiThreads);
         b = g / p.groups_per_req;
         const int jj = g % p.groups_per_req;
@@ -611,6 +760,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         epi_bar(kEpiThreads);
         eg = g;
       }
+      ++run;
+      if (!ok) continue;
       const int tile_c0 = (t - pref[g]) * kBM;  // first column of the tile
       const int64_t c = (int64_t)tile_c0 + m;
       // every row of the group sees the whole tile: no mask, no bounds test
@@ -622,7 +773,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
       if (CONV) {
         const int i = t - t_begin;
         ok = wait_phase(&sfull[i % kScaleRing], (uint32_t)(i / kScaleRing) & 1u, abort_flag, p.fault);
-        if (!ok) break;
+        if (!ok) continue;
         const float sc = scale_ring[(i % kScaleRing) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
@@ -633,14 +784,14 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         const int i = t - t_begin;
         const int st = i % kStages;
         ok = wait_phase(&full[st], (uint32_t)(i / kStages) & 1u, abort_flag, p.fault);
-        if (!ok) break;
+        if (!ok) continue;
         const float sc = *reinterpret_cast<const float*>(S + st * L.stage_bytes + kFp8StageBytes + m * 4);
         ptx::mbar_arrive(&empty[st]);
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
       ok = wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault);
-      if (!ok) break;
+      if (!ok) continue;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
       float* const ob = p.out + (int64_t)r0 * oc + c;  // row r0, this key's column
@@ -697,6 +848,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if (FUSE && eg >= 0) fuse_close(p, pref, eg, run, et, fz, kEpiThreads);
 
     // (2) fp8: this CTA's share of the -inf tail, after its tiles (the
     // converter warps are busy until then).  bf16: the spare warps write it.
@@ -771,6 +923,12 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, (uint32_t)L.tmem_cols);
+  if (FUSE) {
+    // selection of the rows of completed groups: all 512 threads, or the
+    // first 256 of the converter kernel's 448
+    constexpr int NT = kThreads >= 512 ? 512 : 256;
+    if (threadIdx.x < NT) fused_select<NT>(p, pref, G, t_begin, t_end, smem, fz);
+  }
 }
 
 // Launch helpers, one translation unit per key type (umma_bf16.cu, umma_fp8.cu).
@@ -780,11 +938,18 @@ cudaError_t launch_fp8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, 
                        const Layout& L, int grid, cudaStream_t s);
 cudaError_t launch_q8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                       const Layout& L, int grid, cudaStream_t s);
+// Scoring followed by the selection of every row in the same kernel (umma_*_topk.cu).
+cudaError_t launch_bf16_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                             const Layout& L, int grid, cudaStream_t s);
+cudaError_t launch_fp8_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                            const Layout& L, int grid, cudaStream_t s);
+cudaError_t launch_q8_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                           const Layout& L, int grid, cudaStream_t s);
 
-template <int H, int KIND>
+template <int H, int KIND, bool FUSE>
 cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up, const Layout& L,
                      int grid, cudaStream_t s) {
-  auto kern = umma_score_kernel<H, KIND>;
+  auto kern = umma_score_kernel<H, KIND, FUSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
   // programmatic stream serialisation: the launch may begin while the
@@ -804,17 +969,17 @@ cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaPar
   return cudaGetLastError();
 }
 
-template <int KIND>
+template <int KIND, bool FUSE = false>
 cudaError_t launch_any(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                        const Layout& L, int grid, cudaStream_t s) {
   switch (heads) {
-    case 1: return launch_h<1, KIND>(kv, qm, up, L, grid, s);
-    case 2: return launch_h<2, KIND>(kv, qm, up, L, grid, s);
-    case 4: return launch_h<4, KIND>(kv, qm, up, L, grid, s);
-    case 8: return launch_h<8, KIND>(kv, qm, up, L, grid, s);
-    case 16: return launch_h<16, KIND>(kv, qm, up, L, grid, s);
-    case 32: return launch_h<32, KIND>(kv, qm, up, L, grid, s);
-    default: return launch_h<64, KIND>(kv, qm, up, L, grid, s);
+    case 1: return launch_h<1, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 2: return launch_h<2, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 4: return launch_h<4, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 8: return launch_h<8, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 16: return launch_h<16, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 32: return launch_h<32, KIND, FUSE>(kv, qm, up, L, grid, s);
+    default: return launch_h<64, KIND, FUSE>(kv, qm, up, L, grid, s);
   }
 }
 

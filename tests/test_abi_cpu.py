@@ -154,3 +154,30 @@ def test_dispatch_decisions(lib):
         qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256))
     assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
     qsa.force_variant(qsa.VARIANT_AUTO)
+
+
+def test_fused_call_workspace_size_and_argument_checks(lib):
+    """qsa_paged_mqa_topk: host checks before anything is enqueued."""
+    d = _desc()  # 2 requests x 4 rows x 4 heads: one row group a request
+    assert qsa.topk_workspace_bytes(d) == 4 * (2 * 2 + 1)
+    # the CUDA-core scorer's shapes never run the fused selection
+    assert qsa.topk_workspace_bytes(_desc(page_cols=5, key_page_stride=5 * 256)) == 0
+    args = (d, 16, 16, 16, None, 16, 16)
+    for k in (0, 2049):
+        with pytest.raises(qsa.QSAError) as e:
+            qsa.paged_mqa_topk(*args, k, 16, 16, 16, 64, stream=0)
+        assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "k must" in str(e.value)
+    with pytest.raises(qsa.QSAError) as e:  # no workspace
+        qsa.paged_mqa_topk(*args, 8, 16, 16, None, 0, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "workspace" in str(e.value)
+    with pytest.raises(qsa.QSAError) as e:  # workspace too small
+        qsa.paged_mqa_topk(*args, 8, 16, 16, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG and "20 bytes" in str(e.value)
+    with pytest.raises(qsa.QSAError) as e:  # misaligned out_idx
+        qsa.paged_mqa_topk(*args, 8, 16, 18, 16, 64, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+    with pytest.raises(qsa.QSAError) as e:  # the scoring checks come first
+        qsa.paged_mqa_topk(_desc(head_dim=64), 16, 16, 16, None, 16, 16, 8, 16, 16, 16, 64, stream=0)
+    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
+    qsa.paged_mqa_topk(_desc(num_requests=0), None, None, None, None, None, None, 8, None, None, None, 0,
+                       stream=0)  # no rows: nothing to do
