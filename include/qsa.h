@@ -226,6 +226,28 @@ qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* desc, int32_t q_dtype, const
 qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* bytes);
 
 /*
+ * qsa_paged_mqa_topk_noalloc - qsa_paged_mqa_topk with the library's own fixed
+ * counter array in place of the caller's workspace.  The pages have no
+ * counterpart: it exists for callers that want the fused call without owning
+ * device memory for it.  It allocates nothing: the counters are a static
+ * device array of 257 words (row groups of at most 128; qsa_paged_mqa_topk_workspace
+ * > 1028 bytes is rejected with QSA_ERR_UNSUPPORTED before anything is
+ * enqueued).  The array must read zero when a call starts: it is zero when the
+ * library is loaded, and every call that completes leaves it zero (a call
+ * that set qsa_device_status bit 0 may not).  The first call on each device
+ * looks the array's address up (with that device current) and must come
+ * before any stream capture on that device.  Calls that may overlap (other
+ * streams or host threads) share the one array and race: give each of them
+ * qsa_paged_mqa_topk with its own workspace instead.  Arguments, results and
+ * the other errors as qsa_paged_mqa_topk.
+ */
+qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* desc, int32_t q_dtype, const void* q,
+                                      const float* weights, const void* kv_cache, const float* scales,
+                                      const int32_t* block_table, const int32_t* visible_cols,
+                                      const int32_t* next_n_lens, int32_t k, int64_t max_visible,
+                                      float* out_logits, int32_t* out_idx, void* stream);
+
+/*
  * qsa_plan_variant - host-only dispatch decision for `desc` (no CUDA call).
  * Writes the qsa_variant qsa_paged_mqa_logits would launch (honouring
  * qsa_force_variant) to *variant.  The choice uses host metadata only, with no

@@ -22,7 +22,7 @@ VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma", VARIANT_UMMA_
 
 # Every symbol include/qsa.h declares.
 EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_paged_mqa_topk",
-            "qsa_paged_mqa_topk_workspace", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+            "qsa_paged_mqa_topk_workspace", "qsa_paged_mqa_topk_noalloc", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
@@ -67,6 +67,9 @@ def load_library():
         lib.qsa_paged_mqa_topk.restype = ctypes.c_int
         lib.qsa_paged_mqa_topk.argtypes = [ctypes.POINTER(PagedDesc), i32, vp, vp, vp, vp, vp, vp, vp, i32, i64, vp,
                                            vp, vp, ctypes.c_size_t, vp]
+        lib.qsa_paged_mqa_topk_noalloc.restype = ctypes.c_int
+        lib.qsa_paged_mqa_topk_noalloc.argtypes = [ctypes.POINTER(PagedDesc), i32, vp, vp, vp, vp, vp, vp, vp, i32,
+                                                   i64, vp, vp, vp]
         lib.qsa_paged_mqa_topk_workspace.restype = ctypes.c_int
         lib.qsa_paged_mqa_topk_workspace.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(ctypes.c_size_t)]
         lib.qsa_select_topk.restype = ctypes.c_int
@@ -155,6 +158,18 @@ def paged_mqa_topk(desc: PagedDesc, q, weights, kv_cache, scales, block_table, v
                                            _addr(visible_cols), _addr(next_n_lens), int(k), int(max_visible),
                                            _addr(out_logits), _addr(out_idx), _addr(workspace),
                                            int(workspace_bytes), _stream(stream))
+    _check(st)
+
+
+def paged_mqa_topk_noalloc(desc: PagedDesc, q, weights, kv_cache, scales, block_table, visible_cols, k: int,
+                           out_logits, out_idx, stream=None, next_n_lens=None, q_dtype: int = Q_BF16,
+                           max_visible: int = 0) -> None:
+    """qsa_paged_mqa_topk_noalloc: the one-call form with the library's fixed counters."""
+    st = load_library().qsa_paged_mqa_topk_noalloc(ctypes.byref(desc), int(q_dtype), _addr(q), _addr(weights),
+                                                   _addr(kv_cache), _addr(scales), _addr(block_table),
+                                                   _addr(visible_cols), _addr(next_n_lens), int(k),
+                                                   int(max_visible), _addr(out_logits), _addr(out_idx),
+                                                   _stream(stream))
     _check(st)
 
 

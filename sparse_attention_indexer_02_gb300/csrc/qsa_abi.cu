@@ -233,6 +233,33 @@ int64_t fused_words(const qsa_paged_desc* d) {
   return G >= 1 && G <= qsa::kFuseMaxGroups ? 2 * G + 1 : 0;
 }
 
+// Counters of qsa_paged_mqa_topk_noalloc: a fixed array in the library's
+// own device memory instead of a caller workspace (zero when the library is
+// loaded; every completed call leaves it zero).
+constexpr int kNoAllocGroups = 128;
+constexpr int kNoAllocWords = 2 * kNoAllocGroups + 1;
+static __device__ __align__(256) uint32_t g_noalloc_counters[kNoAllocWords];
+
+// Device address of g_noalloc_counters on the current device, looked up once
+// per device (with that device current).
+cudaError_t noalloc_counters(uint32_t** out) {
+  static std::mutex mu;
+  static uint32_t* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_noalloc_counters);
+    if (e != cudaSuccess) return e;
+    addr[dev] = static_cast<uint32_t*>(a);
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -304,6 +331,29 @@ qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* d, int32_t q_dtype, const vo
                                    p.capacity, k, out_idx, s);
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
+}
+
+qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* d, int32_t q_dtype, const void* q,
+                                      const float* weights, const void* kv_cache, const float* scales,
+                                      const int32_t* block_table, const int32_t* visible_cols,
+                                      const int32_t* next_n_lens, int32_t k, int64_t max_visible,
+                                      float* out_logits, int32_t* out_idx, void* stream) {
+  qsa_status st = validate_desc(d);
+  if (st != QSA_OK) return st;
+  const int64_t words = fused_words(d);
+  if (words > kNoAllocWords)
+    return fail(QSA_ERR_UNSUPPORTED,
+                "qsa_paged_mqa_topk_noalloc holds counters for %d row groups and this shape has %lld: "
+                "call qsa_paged_mqa_topk with a workspace of %lld bytes",
+                kNoAllocGroups, (long long)(words - 1) / 2, (long long)words * 4);
+  uint32_t* counters = nullptr;
+  if (words > 0) {
+    cudaError_t e = noalloc_counters(&counters);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "counter address: %s", cudaGetErrorString(e));
+  }
+  return qsa_paged_mqa_topk(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols, next_n_lens, k,
+                            max_visible, out_logits, out_idx, counters, words > 0 ? sizeof(g_noalloc_counters) : 0,
+                            stream);
 }
 
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear) {

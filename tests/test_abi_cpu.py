@@ -181,3 +181,15 @@ def test_fused_call_workspace_size_and_argument_checks(lib):
     assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
     qsa.paged_mqa_topk(_desc(num_requests=0), None, None, None, None, None, None, 8, None, None, None, 0,
                        stream=0)  # no rows: nothing to do
+
+
+def test_noalloc_call_rejects_shapes_past_its_counters(lib):
+    """qsa_paged_mqa_topk_noalloc holds counters for 128 row groups: a larger
+    shape is refused before anything is enqueued."""
+    d = _desc(num_requests=200, rows_per_req=1)  # 200 groups of one row
+    with pytest.raises(qsa.QSAError) as e:
+        qsa._abi.paged_mqa_topk_noalloc(d, 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "128 row groups" in str(e.value)
+    with pytest.raises(qsa.QSAError) as e:  # the scoring checks come first
+        qsa._abi.paged_mqa_topk_noalloc(_desc(head_dim=64), 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "head_dim" in str(e.value)
