@@ -2,7 +2,9 @@
 """Benchmark of the QSA-indexer hot path: paged MQA-logits scoring + top-k.
 
 One step = qsa_paged_mqa_logits + qsa_select_topk over one batch of the
-workload (two kernel launches).  Prints one JSON line.
+workload (two kernel launches; with --step fused one qsa_paged_mqa_topk call,
+the selection inside the scoring kernel for decode-sized calls).  Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -127,7 +129,9 @@ def source_sha(paths):
 KERNEL_SOURCES = {
     "rowcore": ["sparse_attention_indexer_02_gb300/csrc/rowcore.cu"],
     "umma": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
-    "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu"],
+    "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu", "sparse_attention_indexer_02_gb300/csrc/topk_select.cuh"],
+    "umma+topk": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu",
+                  "sparse_attention_indexer_02_gb300/csrc/topk_select.cuh"],
 }
 
 
@@ -387,10 +391,13 @@ def run_gpu(args):
     # eager warm-up (first calls set kernel attributes), then CUDA graphs: the
     # host enqueues one graph per >= 16 steps, so launch overhead on the host
     # never shows up in the device timings.
+    fused_step = args.step == "fused"
     for i in range(args.warmup):
         d = sets[i % copies]
         score(d)
         topk(d)
+        if fused_step:
+            fused(d)
     variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
     torch.cuda.synchronize(dev)
 
@@ -399,6 +406,9 @@ def run_gpu(args):
         with torch.cuda.graph(g):
             for i in range(n_steps):
                 d = sets[i % copies]
+                if do_score and do_topk and fused_step:
+                    fused(d)
+                    continue
                 if do_score:
                     score(d)
                 if do_topk:
@@ -472,7 +482,9 @@ def run_gpu(args):
     # roofline of the dominant kernel
     peaks = measured_peaks()
     sb, tb = algorithmic_bytes(spec)
-    if score_us >= topk_us:
+    if fused_step:  # one kernel: its bytes are the scoring's and the selection's
+        kname, kbytes, kus = variant, sum(sb.values()) + sum(tb.values()), fused_us
+    elif score_us >= topk_us:
         kname, kbytes, kus = variant, sum(sb.values()), score_us
     else:
         kname, kbytes, kus = "topk", sum(tb.values()), topk_us
@@ -494,8 +506,11 @@ def run_gpu(args):
         for _ in range(3):
             for name, t in host.items():
                 d[name].copy_(t, non_blocking=True)
-            score(d)
-            topk(d)
+            if fused_step:
+                fused(d)
+            else:
+                score(d)
+                topk(d)
             out_host.copy_(d["idx"], non_blocking=True)
         torch.cuda.synchronize(dev)
         barrier()
@@ -504,8 +519,11 @@ def run_gpu(args):
         for _ in range(Ke):
             for name, t in host.items():
                 d[name].copy_(t, non_blocking=True)
-            score(d)
-            topk(d)
+            if fused_step:
+                fused(d)
+            else:
+                score(d)
+                topk(d)
             out_host.copy_(d["idx"], non_blocking=True)
         e1.record(torch.cuda.current_stream(dev))
         torch.cuda.synchronize(dev)
@@ -532,7 +550,7 @@ def run_gpu(args):
             "step_us": round(1e3 * ms_step, 3),
             "fused_step_us": round(fused_us, 3), "fused_variant": fused_variant,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 2 * K, "clocks": clocks,
+            "gpu_launches": (1 if fused_step else 2) * K, "clocks": clocks,
         }
         print(json.dumps(line))
     if world > 1:
@@ -548,6 +566,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(qi.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", choices=["auto", "rowcore", "umma"], default="auto")
+    ap.add_argument("--step", choices=["two-call", "fused"], default="two-call",
+                    help="time the step as qsa_paged_mqa_logits + qsa_select_topk, or as one qsa_paged_mqa_topk")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
