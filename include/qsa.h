@@ -209,8 +209,9 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
  *   workspace    device memory of at least qsa_paged_mqa_topk_workspace(desc)
  *                bytes, 4-byte aligned (NULL when that size is 0).  It must
  *                hold zeros before the first call; every completed call leaves
- *                it zero again.  Calls that may run at the same time (other
- *                streams) need their own workspaces.
+ *                it zero again (a call that set qsa_device_status bit 0 may
+ *                not: zero it before the next call).  Calls that may run at the
+ *                same time (other streams) need their own workspaces.
  * Errors as qsa_paged_mqa_logits_ex; k out of range, a NULL or misaligned
  * out_idx, or a missing or short workspace: QSA_ERR_INVALID_ARG.
  */
