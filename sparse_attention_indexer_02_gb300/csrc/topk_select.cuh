@@ -147,7 +147,9 @@ struct Segment {
   }
 };
 
-// Exclusive prefix of v over the NT selecting threads, and the total.
+// Exclusive prefix of v over the NT selecting threads, and the total.  The
+// warp totals are read after the one barrier; callers put a barrier between
+// two calls (every caller does), so the next call cannot overwrite them early.
 template <int NT>
 __device__ __forceinline__ int block_excl_sum(int v, int32_t* warp_tot, int* total) {
   constexpr int kW = NT / 32;
@@ -169,7 +171,6 @@ __device__ __forceinline__ int block_excl_sum(int v, int32_t* warp_tot, int* tot
   }
   const int warp_excl = __shfl_sync(0xFFFFFFFFu, wincl - t, warp);
   *total = __shfl_sync(0xFFFFFFFFu, wincl, 31);
-  bar_sync<NT>();
   return warp_excl + incl - v;
 }
 
@@ -255,7 +256,9 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* hist, uint32_t* acc,
 // is needed, and thread order is column order: one exclusive scan of each
 // thread's (above, equal) counts gives every thread its first output slot.
 // (Staging the row and the output through shared memory for coalesced global
-// accesses measured slower for rows of 2K to 8K columns.)
+// accesses, and writing each warp's run of output slots coalesced with a
+// shuffle search for each slot's owner lane, both measured slower for rows of
+// 2K to 8K columns than these per-thread stores.)
 // Shared memory at `dyn`: three histograms (2048 + 2048 + 1024 words).
 constexpr int kRegHistWords = 2 * kBins + 1024;
 

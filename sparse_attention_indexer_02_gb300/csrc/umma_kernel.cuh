@@ -64,6 +64,7 @@ struct Roles {
 };
 constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kFastSchedRows = 256;              // up to this many rows one warp builds the schedule
+constexpr int64_t kPrefetchLines = 8192;         // block-table lines warmed in L2 before the wait (1 MB)
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in limit per CTA
 // Fused selection: at most kFuseMaxGroups row groups (their counters live in
 // the caller's workspace, the list of groups a CTA completed in shared memory).
@@ -449,8 +450,23 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     ptx::prefetch_tmap(&kv_map);
     ptx::prefetch_tmap(&q_map);
   }
+  // Warm L2 with the visible counts and the block table (a share of their
+  // 128-byte lines per CTA, at most kPrefetchLines in all) while the previous
+  // kernel finishes: a prefetch returns no data, so running ahead of that
+  // kernel's writes cannot be observed, and every load below comes after the wait.
+  if (warp >= 2) {
+    const int64_t vis_lines = ((int64_t)p.num_rows * 4 + 127) / 128;
+    const int64_t bt_bytes = (int64_t)(p.num_rows / p.rows_per_req) * p.max_pages * 4;
+    const int64_t bt_lines = min((bt_bytes + 127) / 128, kPrefetchLines);
+    for (int64_t l = blockIdx.x + (int64_t)gridDim.x * (threadIdx.x - 64); l < vis_lines + bt_lines;
+         l += (int64_t)gridDim.x * (kThreads - 64)) {
+      const char* a = l < vis_lines ? reinterpret_cast<const char*>(p.visible) + l * 128
+                                    : reinterpret_cast<const char*>(p.block_table) + (l - vis_lines) * 128;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
+    }
+  }
   // Everything above overlaps the previous kernel in the stream; no global
-  // memory is touched before it has completed.
+  // memory is loaded before it has completed.
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   int32_t vfast[kFastSchedRows / 32], nfast[kFastSchedRows / 32];
