@@ -10,7 +10,7 @@
 // reduces heads in registers, and its stores of one row are 32 consecutive
 // floats per warp.
 //
-// Structure (one persistent CTA per SM, 10 warps):
+// Structure (one persistent CTA per SM, 16 warps; 14 with the converter):
 //  * schedule: every CTA derives, from the visible counts, the tile count of
 //    each row group (tiles past the group's widest visible column are never
 //    scheduled - the early exit of vLLM #62589 "Overview") and takes an equal
@@ -27,6 +27,10 @@
 //    every third row block of the group; four warps with the converter):
 //    tcgen05.ld of the tile's columns, per head ReLU * weight, head sum,
 //    +0.0, -inf past the row's visible count, store.
+//  * warps 14-15 (bf16 keys or fp8 q): the -inf tail; with fp8 keys and bf16
+//    q, warps 6-13 instead widen each e4m3 key tile to bf16 for the MMA.
+//  * FUSE instantiations (qsa_paged_mqa_topk) then select the rows of the row
+//    groups whose last tile this CTA stored (see "fused selection" below).
 // Every barrier wait gives up after about a second, sets the device fault
 // word (qsa_device_status) and lets the CTA drain and exit.
 #pragma once

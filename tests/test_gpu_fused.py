@@ -215,5 +215,18 @@ def test_fused_graph_replay_with_new_inputs(oracle_mod):
         assert workspace_is_zero()
 
 
+@pytest.mark.parametrize("name", ["single_row_decode", "tiny_mtp"])
+def test_fused_full_size_decode_workloads(oracle_mod, name):
+    """The one-call form at the full size the bench times it (its host bound of
+    the visible counts, so the selection runs in the scoring kernel): every
+    row's logits and selection against the oracle."""
+    spec = qi.WORKLOADS[name]()
+    inp = qi.build_inputs(spec)
+    logits, idx, ran, _ = run_fused(inp, spec.k, max_visible=int(spec.live_visible().max()))
+    assert ran == qsa.VARIANT_UMMA_TOPK
+    check(oracle_mod, inp, logits, idx, spec.k, where=f"{name} full size")
+    assert workspace_is_zero()
+
+
 def test_no_fused_kernel_gave_up_on_a_barrier():
     assert qsa.device_status(clear=True) == 0
