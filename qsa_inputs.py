@@ -263,6 +263,14 @@ def prefill_chunk() -> Spec:
                 BASE_SEED + 4)
 
 
+def prefill_chunk_4k() -> Spec:
+    """The last 4,096 rows of prefill_chunk (positions 94,208..98,303): the same tile shape
+    (64 rows x 4 heads = N 256) on a quarter of the logits, small enough for a full
+    profiler capture."""
+    vis = prefill_visible(94208, 4096)
+    return Spec("prefill_4096rows_at_94208_p64", 1, 4096, 4, 64, 24576, 2048, KV_BF16, vis, BASE_SEED + 6)
+
+
 def ragged_nn8() -> Spec:
     """aiter #4221 ragged mix: 116 requests x next_n 8, next_n_lens ~ U{1..8}, fp8 q and
     fp8 block-flat keys (KV block 64), 32 heads, prompts ~ U[32K, 128K] tokens, k 2048."""
@@ -290,6 +298,7 @@ WORKLOADS = {
     "mtp3_large_p64": lambda: mtp3_large(64),
     "fp8_h64": fp8_h64,
     "prefill_chunk": prefill_chunk,
+    "prefill_chunk_4k": prefill_chunk_4k,
     "ragged_nn8": ragged_nn8,
     "fp8q_h64": fp8q_h64,
 }

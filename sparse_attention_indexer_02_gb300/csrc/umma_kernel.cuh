@@ -395,7 +395,9 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
   const int N = L.n;
   const int kStages = L.stages;
   const int kAStages = L.a_stages;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-byte aligned base, by an offset from the shared-memory symbol (not an
+  // integer round trip) so every pointer below is known to address shared memory
+  uint8_t* smem = smem_raw + ((1024u - (ptx::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* S = smem;                          // TMA stages
   uint8_t* A = CONV ? smem + L.a_off : smem;  // MMA A-operand stages (128-byte swizzle)
   uint8_t* Bq = smem + L.b_off;
