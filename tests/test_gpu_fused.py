@@ -215,6 +215,20 @@ def test_fused_graph_replay_with_new_inputs(oracle_mod):
         assert workspace_is_zero()
 
 
+def test_fused_call_with_the_cuda_core_scorer(oracle_mod):
+    """A forced CUDA-core scorer makes the call the scoring launch + the top-k
+    launch (the fused selection lives in the tcgen05 kernel only)."""
+    inp = qi.build_inputs(case_spec(CASES[2], qi.KV_BF16))
+    qsa.force_variant(qsa.VARIANT_ROWCORE)
+    try:
+        logits, idx, ran, _ = run_fused(inp, inp.spec.k, max_visible=int(inp.spec.visible.max()))
+    finally:
+        qsa.force_variant(qsa.VARIANT_AUTO)
+    assert ran == qsa.VARIANT_ROWCORE
+    check(oracle_mod, inp, logits, idx, inp.spec.k, where="rowcore composition")
+    assert workspace_is_zero()
+
+
 @pytest.mark.parametrize("name", ["single_row_decode", "tiny_mtp"])
 def test_fused_full_size_decode_workloads(oracle_mod, name):
     """The one-call form at the full size the bench times it (its host bound of
