@@ -175,6 +175,10 @@ qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* desc, int32_t q_dtype, 
  * Arguments (device pointers): logits fp32 rows of row_stride floats;
  * visible_cols int32 [num_rows]; out_idx int32 [num_rows][k].
  * num_rows >= 0, row_stride >= 1, 1 <= k <= 2048.
+ * The kernel is launched with programmatic stream serialisation and reads
+ * visible_cols before it waits for the kernel before it in the stream (the
+ * logits after): visible_cols must not be written by that kernel.  The
+ * library's scoring kernels never write it.
  */
 qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
                            const int32_t* visible_cols, int32_t k, int32_t* out_idx,

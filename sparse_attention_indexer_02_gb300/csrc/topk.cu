@@ -38,8 +38,6 @@ template <bool CLUSTER>
 __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
   extern __shared__ uint4 dyn_topk[];
   __shared__ Shared sh;
-  ptx::grid_dep_wait();  // the logits come from the previous kernel in the stream
-  ptx::grid_dep_launch();
   int CL = 1, rank = 0;  // cluster size and this CTA's rank in it
   if (CLUSTER) {
     cg::cluster_group cl = cg::this_cluster();
@@ -47,7 +45,13 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
     rank = (int)cl.block_rank();
   }
   const int64_t row = blockIdx.x / CL;
+  // The row's visible count is read while the previous kernel may still run:
+  // a kernel lets this one start early only after its own dependency wait, and
+  // the scoring kernels that precede it never write the counts (the contract
+  // of qsa_select_topk states it).  The logits are read after the wait.
   const int n = (int)row_visible(a.visible, a.next_n_lens, row, a.rows_per_req, a.capacity);
+  ptx::grid_dep_wait();
+  ptx::grid_dep_launch();
   const RowTask task{a.logits + row * a.row_stride, n, a.out + row * (int64_t)a.k};
   const Config cf{a.k, a.cap, a.cpw, a.bulk, a.fault};
   select_row<kT, CLUSTER, false, kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh, CL, rank);
