@@ -89,7 +89,7 @@ TopkPlan plan_for(int C, int64_t row_stride) {
   const int64_t room = (kSmemMax - fixed - 4LL * kW * cpw) / 4;
   if (cap > room) cap = room & ~int64_t(3);
   size_t bytes = (size_t)(4 * (cap + kW * cpw) + fixed);
-  const size_t reg = 4 * (size_t)kRegHistWords;  // short rows: keys in registers
+  const size_t reg = 4 * (size_t)(kRegHistWords + (C > 1 ? kAccWords : 0));  // keys in registers
   return TopkPlan{cap, cpw, bytes > reg ? bytes : reg};
 }
 

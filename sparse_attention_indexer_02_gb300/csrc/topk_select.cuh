@@ -248,34 +248,49 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* hist, uint32_t* acc,
   bar_sync<NT>();
 }
 
-// ---- register-resident selection of a short row ------------------------------
-// A row of n <= NT * KPT columns, one CTA: with q = ceil(n / NT) <= KPT,
-// thread t holds the keys of columns [t * q, t * q + q) in registers (every
-// thread has keys, however short the row), so every digit's histogram is a
-// scan of registers (the keys of the current prefix only), no candidate list
-// is needed, and thread order is column order: one exclusive scan of each
-// thread's (above, equal) counts gives every thread its first output slot.
+// ---- register-resident selection ---------------------------------------------
+// A CTA's segment of at most NT * KPT columns (a row one CTA selects alone, or
+// one CTA's share of a row a cluster splits): with q = ceil(len / NT) <= KPT,
+// thread t holds the keys of segment columns [t * q, t * q + q) in registers
+// (every thread has keys, however short the segment), so every digit's
+// histogram is a scan of registers (the keys of the current prefix only), no
+// candidate list is needed, and thread order is column order: one exclusive
+// scan of each thread's (above, equal) counts gives every thread its first
+// output slot.  In a cluster the histograms are summed over distributed shared
+// memory and the CTAs' counts exchanged exactly as in the compaction path
+// below (one cluster barrier per digit and one for the counts).
 // (Staging the row and the output through shared memory for coalesced global
 // accesses, and writing each warp's run of output slots coalesced with a
 // shuffle search for each slot's owner lane, both measured slower for rows of
 // 2K to 8K columns than these per-thread stores.)
-// Shared memory at `dyn`: three histograms (2048 + 2048 + 1024 words).
+// Shared memory at `dyn`: three histograms (2048 + 2048 + 1024 words), then in
+// a cluster the per-digit accumulators (kAccWords).
 constexpr int kRegHistWords = 2 * kBins + 1024;
 
-template <int NT, int KPT, bool COHERENT>
-__device__ __forceinline__ void select_row_reg(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh) {
+template <int NT, int KPT, bool COHERENT, bool CLUSTER>
+__device__ __forceinline__ void select_row_reg(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh,
+                                               int C, int part) {
   static_assert(KPT % 4 == 0, "keys per thread in groups of 4");
   const int tid = (int)threadIdx.x;
+  const int lane = lane_id();
+  const bool multi = CLUSTER && C > 1;  // the same in every CTA of the cluster
   const int n = task.n, k = cf.k;
-  const float* x = task.row;
+  // this CTA's segment [s0, s0 + len) of the row; boundaries on multiples of 4
+  const int per_cta = ((n + C - 1) / C + 3) & ~3;
+  const int s0 = min(n, part * per_cta);
+  const int len = min(n, s0 + per_cta) - s0;
+  const float* x = task.row + s0;
   uint32_t* h0 = dyn;
   uint32_t* h1 = h0 + kBins;
   uint32_t* h2 = h1 + kBins;
+  uint32_t* acc = dyn + kRegHistWords;  // cluster: the three digits' accumulators
   for (int i = tid; i < kRegHistWords; i += NT) h0[i] = 0;
+  if (multi)
+    for (int i = tid; i < kAccWords; i += NT) acc[i] = 0;
   // this thread's keys; slots past its columns hold key 0 and are never counted
-  const int q = (n + NT - 1) / NT;
+  const int q = (len + NT - 1) / NT;
   const int c0 = tid * q;
-  const int mine = max(0, min(q, n - c0));  // valid keys of this thread
+  const int mine = max(0, min(q, len - c0));  // valid keys of this thread
   uint32_t key[KPT];
   if ((q & 3) == 0 && (reinterpret_cast<uintptr_t>(x + c0) & 15u) == 0) {
 #pragma unroll
@@ -291,11 +306,16 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
 #pragma unroll
     for (int j = 0; j < KPT; ++j) key[j] = j < mine ? topk_key(ld_row1<COHERENT>(x + c0 + j)) : 0u;
   }
-  bar_sync<NT>();  // histograms zeroed
+  bar_sync<NT>();  // histograms (and accumulators) zeroed
+  if (multi) cluster_arrive();  // accumulators zeroed (waited for before the first push)
 #pragma unroll
   for (int j = 0; j < KPT; ++j)
     if (j < mine) atomicAdd(&h0[key[j] >> 21], 1u);
   bar_sync<NT>();
+  if (multi) {
+    cluster_wait();
+    cluster_sum<NT>(h0, acc, h0, kBins, C);
+  }
   int remaining = k;
   find_digit<NT>(sh, h0, kBins, remaining);
   bar_sync<NT>();
@@ -305,6 +325,7 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
   for (int j = 0; j < KPT; ++j)
     if (j < mine && (key[j] >> 21) == d0) atomicAdd(&h1[(key[j] >> 10) & 2047u], 1u);
   bar_sync<NT>();  // every thread has read sh for d0; h1 complete
+  if (multi) cluster_sum<NT>(h1, acc + kBins, h1, kBins, C);
   find_digit<NT>(sh, h1, kBins, remaining);
   bar_sync<NT>();
   const uint32_t p22 = (d0 << 11) | (uint32_t)sh.digit;
@@ -313,6 +334,7 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
   for (int j = 0; j < KPT; ++j)
     if (j < mine && (key[j] >> 10) == p22) atomicAdd(&h2[key[j] & 1023u], 1u);
   bar_sync<NT>();
+  if (multi) cluster_sum<NT>(h2, acc + 2 * kBins, h2, 1024, C);
   find_digit<NT>(sh, h2, 1024, remaining);
   bar_sync<NT>();
   // the k-th largest key; of the keys equal to it the `remaining` lowest columns are kept
@@ -328,8 +350,29 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
   int tot;
   const int ex = block_excl_sum<NT>((gt << 16) | eq, sh.warp_tot, &tot);
   const int gt_before = ex >> 16, eq_before = ex & 0xFFFF;
-  int pos = gt_before + min(eq_before, remaining);  // selected columns before this thread's
-  int eq_rank = eq_before;
+  // the CTAs before this one in the cluster: keys above the threshold, keys equal to it
+  int gt_ctas = 0, eq_ctas = 0;
+  if (multi) {
+    cg::cluster_group cl = cg::this_cluster();
+    if (tid == 0) {
+      sh.cta_gt = tot >> 16;
+      sh.cta_eq = tot & 0xFFFF;
+    }
+    cl.sync();
+    int qg = 0, qe = 0;
+    if (lane < part) {  // part < C <= 8
+      qg = *cl.map_shared_rank(&sh.cta_gt, lane);
+      qe = *cl.map_shared_rank(&sh.cta_eq, lane);
+    }
+    __syncwarp();
+    cluster_arrive();  // done with remote shared memory (waited for before exit)
+    gt_ctas = __reduce_add_sync(0xFFFFFFFFu, qg);
+    eq_ctas = __reduce_add_sync(0xFFFFFFFFu, qe);
+  }
+  // selected columns before this thread's: every larger key, and of the equal
+  // keys (row order) the first `remaining`
+  int pos = gt_ctas + gt_before + min(eq_ctas + eq_before, remaining);
+  int eq_rank = eq_ctas + eq_before;
   int32_t* o = task.out;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
@@ -337,9 +380,14 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
     const bool take = (j < mine && key[j] > thr) || (is_eq && eq_rank < remaining);
     eq_rank += (int)is_eq;
     if (take) {
-      if (pos < k) o[pos] = c0 + j;
+      if (pos < k) o[pos] = s0 + c0 + j;
       ++pos;
     }
+  }
+  // no CTA leaves while another may still read its shared memory
+  if (multi) {
+    __syncwarp();
+    cluster_wait();
   }
 }
 
@@ -352,7 +400,8 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
 // COHERENT: the logits were written by other CTAs of the running kernel
 // (plain loads coherent at L2; cf.bulk must be 0).  KPT > 0: a row one CTA
 // selects alone and that has at most NT * KPT columns takes select_row_reg
-// (`dyn` must then hold kRegHistWords words).  The caller separates
+// (`dyn` must then hold kRegHistWords words, kRegHistWords + kAccWords in a
+// cluster).  The caller separates
 // two calls on the same shared memory with a barrier of the NT threads.
 template <int NT, bool CLUSTER, bool COHERENT, int KPT = 0>
 __device__ __forceinline__ void select_row(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh,
@@ -381,9 +430,16 @@ __device__ __forceinline__ void select_row(const RowTask& task, const Config& cf
   // the decision depends on the row only, so it is the same in every CTA.
   const bool multi = CLUSTER && n > kSoloMax;
   if (CLUSTER && !multi && rank != 0) return;
-  if (KPT > 0 && !multi && n <= NT * KPT) {  // short row: keys in registers
-    select_row_reg<NT, (KPT > 0 ? KPT : 4), COHERENT>(task, cf, dyn, sh);
-    return;
+  if (KPT > 0) {  // segments of at most NT * KPT columns: keys in registers
+    constexpr int K4 = KPT > 0 ? KPT : 4;
+    if (!multi && n <= NT * KPT) {  // one CTA (its own instantiation: no cluster code in it)
+      select_row_reg<NT, K4, COHERENT, false>(task, cf, dyn, sh, 1, 0);
+      return;
+    }
+    if (multi && (((n + CL - 1) / CL + 3) & ~3) <= NT * KPT) {  // the same in every CTA of the cluster
+      select_row_reg<NT, K4, COHERENT, CLUSTER>(task, cf, dyn, sh, CL, rank);
+      return;
+    }
   }
   const int C = multi ? CL : 1;
   const int part = multi ? rank : 0;
