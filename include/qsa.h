@@ -2,7 +2,10 @@
  * qsa.h - C ABI of the GB300 (sm_103a) QSA-indexer library: paged MQA-logits
  * scoring and per-row top-k selection.
  *
- * The two compute calls follow the problem statement of the pages:
+ * The compute calls - scoring (qsa_paged_mqa_logits and its _ragged / _ex
+ * forms), selection (qsa_select_topk) and both in one call
+ * (qsa_paged_mqa_topk, qsa_paged_mqa_topk_noalloc) - follow the problem
+ * statement of the pages:
  *   - vLLM #62589 "Tile QSA indexer scoring and skip invisible columns",
  *     Dispatch and Details: qsa_mqa_paged(...) scores request-major query rows
  *     against a paged compressed-key cache; top_k_per_row_decode reads
@@ -19,8 +22,9 @@
  *     caller; the library never frees or retains them.  `desc` is host memory,
  *     read during the call only.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is
- *     enqueued asynchronously; no call synchronises the host with the device,
- *     so both calls can be captured in a CUDA graph.
+ *     enqueued asynchronously; no compute call synchronises the host with the
+ *     device, so they can be captured in a CUDA graph (the first call of
+ *     qsa_paged_mqa_topk_noalloc on a device excepted, see there).
  *   - The library allocates no device memory per call.
  *   - Argument errors are detected on the host, before anything is enqueued,
  *     and returned synchronously (QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED);
