@@ -831,6 +831,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         for (int q = 0; q < kUnitsPerBatch; ++q) {
           const int u = u0 + kHalves * q;
           if (u >= nunits) break;
+          // the unit's first row; its rows are constant offsets from it
+          float* const obu = ob + (int64_t)(u * kRowsPerUnit) * oc;
 #pragma unroll
           for (int rr = 0; rr < kRowsPerUnit; ++rr) {
             const int j = u * kRowsPerUnit + rr;
@@ -851,7 +853,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
               part = fmaf(wh, relu_nan(xv), part);
             }
             if (FP8) part *= mag;
-            float* const dst = ob + (int64_t)j * oc;
+            float* const dst = obu + (int64_t)rr * oc;
             if (unmasked) {
               if (stream_out) __stcs(dst, part + 0.0f);
               else *dst = part + 0.0f;
