@@ -63,14 +63,18 @@ namespace {
 
 // Shared-memory plan of one launch: the segment cache, per-warp candidate
 // lists and the histograms.  One CTA a row aims at two CTAs per SM (lists of
-// at least 64 entries a warp); a cluster launch keeps one CTA per SM (its
-// solo rows then never share an SM) and kCpwMax-entry lists.
+// at least 64 entries a warp); when a whole row does not fit that budget it
+// is cached whole at one CTA per SM, unless the rows outnumber the SMs
+// (`waves`): then two CTAs an SM cache part of their rows (the rest is read
+// back from L2) and the launch takes half the waves.  A cluster launch keeps
+// one CTA per SM (its solo rows then never share an SM) and kCpwMax-entry
+// lists.
 struct TopkPlan {
   int64_t cap, cpw;
   size_t smem;
 };
 
-TopkPlan plan_for(int C, int64_t row_stride) {
+TopkPlan plan_for(int C, int64_t row_stride, bool waves = false) {
   int64_t per_cta = ((row_stride + C - 1) / C + 3) & ~int64_t(3);
   if (C > 1) {  // a solo row is cached whole
     const int64_t solo = ((row_stride < kSoloMax ? row_stride : kSoloMax) + 3) & ~int64_t(3);
@@ -81,6 +85,11 @@ TopkPlan plan_for(int C, int64_t row_stride) {
   int64_t cpw = kCpwMax;
   if (C == 1) {
     const int64_t two_per_sm = 110LL * 1024;
+    if (waves && 4 * cap + fixed + 4LL * kW * 64 > two_per_sm) {
+      cpw = 256;
+      cap = ((two_per_sm - fixed - 4LL * kW * cpw) / 4) & ~int64_t(3);
+      return TopkPlan{cap, cpw, (size_t)(4 * (cap + kW * cpw) + fixed)};
+    }
     if (4 * cap + fixed + 4LL * kW * 64 <= two_per_sm) {
       cpw = ((two_per_sm - 4 * cap - fixed) / (4LL * kW)) & ~int64_t(3);
       if (cpw > kCpwMax) cpw = kCpwMax;
@@ -158,7 +167,10 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
         break;
       }
     }
-  const TopkPlan pl = plan_for(C, row_stride);
+  DeviceInfo dinfo;
+  e = device_info(&dinfo);
+  if (e != cudaSuccess) return e;
+  const TopkPlan pl = plan_for(C, row_stride, num_rows > dinfo.num_sms);
   TopkArgs a;
   a.logits = logits;
   a.row_stride = row_stride;
