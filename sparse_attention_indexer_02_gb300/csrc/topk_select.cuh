@@ -9,7 +9,9 @@
 //
 // A row is split over C CTAs (C = 1, or a thread-block cluster of 2, 4 or 8
 // when there are few rows for the GPU and the row is longer than 16384
-// columns), each owning a contiguous segment of the row.  Per CTA:
+// columns), each owning a contiguous segment of the row.  A segment of at
+// most 8192 columns (16 a thread) is selected with its keys in registers
+// (select_row_reg below).  Longer segments take the compaction path, per CTA:
 //  1. The segment is copied into shared memory (16 KB bulk copies with an
 //     mbarrier per chunk, or plain loads) and turned in place into
 //     order-preserving uint32 keys while the top 11 key bits are counted in a
