@@ -118,11 +118,38 @@ def algorithmic_bytes(spec: qi.Spec):
     return score, topk
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without // and /* */ comments (string and character
+    literals kept) and without blank lines or trailing spaces: what the
+    compiler sees, so a comment edit leaves a kernel's recorded counters valid."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = (line.rstrip() for line in "".join(out).splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_sha(paths):
+    """Hash of the kernel sources as compiled (comments and blank lines aside)."""
     h = hashlib.sha256()
     for p in paths:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 
