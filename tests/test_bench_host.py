@@ -1,0 +1,23 @@
+"""bench.py host helpers that need no GPU: the kernel-source hash behind the
+recorded DRAM traffic ignores comments and layout but not code."""
+import bench
+
+
+def test_strip_comments_keeps_code_and_literals():
+    src = ('int a = 1; // trailing\n/* block\n   comment */ const char* s = "x // not a comment";\n'
+           "char q = '\\'';  \n\n  /* one */ int b; /* two */\n")
+    out = bench.strip_comments(src)
+    assert "trailing" not in out and "block" not in out and "one" not in out and "two" not in out
+    assert '"x // not a comment"' in out and "'\\''" in out
+    assert "int a = 1;" in out and "int b;" in out
+    assert "\n\n" not in out and not any(line != line.rstrip() for line in out.splitlines())
+
+
+def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "k.cu").write_text("// header\n__global__ void k(int* p) { p[0] = 1; }\n")
+    a = bench.source_sha(["k.cu"])
+    (tmp_path / "k.cu").write_text("/* another header */\n__global__ void k(int* p) { p[0] = 1; }  // note\n\n")
+    assert bench.source_sha(["k.cu"]) == a
+    (tmp_path / "k.cu").write_text("__global__ void k(int* p) { p[0] = 2; }\n")
+    assert bench.source_sha(["k.cu"]) != a
