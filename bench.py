@@ -101,7 +101,11 @@ def measured_peaks():
 
 
 def algorithmic_bytes(spec: qi.Spec):
-    """Bytes each kernel must move at least once per launch."""
+    """Bytes each kernel must move at least once per launch.  Scorer: each
+    request's visible key columns once (fp8 scales included), q, the weights,
+    the block-table entries of the pages read, the visible counts and the
+    logits written.  Top-k: the visible logits read, the counts and the
+    indices written."""
     R, H = spec.num_rows, spec.num_heads
     pages = int(spec.pages_needed().sum())
     score = {
