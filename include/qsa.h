@@ -26,6 +26,15 @@
  *     device, so they can be captured in a CUDA graph (the first call of
  *     qsa_paged_mqa_topk_noalloc on a device excepted, see there).
  *   - The library allocates no device memory per call.
+ *   - Kernels are launched with programmatic stream serialisation: a call's
+ *     kernel may start while the kernel before it in the stream is still
+ *     running, and it waits for that kernel before it reads q, weights, keys,
+ *     scales or logits and before it writes anything.  The row metadata -
+ *     visible_cols, next_n_lens and block_table - may be read before that
+ *     wait, so the kernel just before a compute call in its stream must not
+ *     write them (copies, and kernels further back in the stream, may).  The
+ *     library's own kernels never write them, and each of them waits for its
+ *     own predecessor before it lets the next kernel start.
  *   - Argument errors are detected on the host, before anything is enqueued,
  *     and returned synchronously (QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED);
  *     a failed launch returns QSA_ERR_CUDA.  qsa_last_error() describes the
@@ -115,7 +124,8 @@ typedef struct qsa_paged_desc {
  *                rejected as mixed operand types, as SGLang #48649's
  *                rejects_mixed_operand_dtypes test does).
  *   block_table  int32 [num_requests][max_pages] physical page ids; only the
- *                entries covering a request's visible columns are read.
+ *                entries covering a request's visible columns are read.  Read
+ *                early (see the conventions above), as is visible_cols.
  *   visible_cols int32 [R] visible column count of each row.
  *   out_logits   fp32 [R][out_cols]; every element is written.
  *   stream       cudaStream_t.
@@ -179,10 +189,8 @@ qsa_status qsa_paged_mqa_logits_ex(const qsa_paged_desc* desc, int32_t q_dtype, 
  * Arguments (device pointers): logits fp32 rows of row_stride floats;
  * visible_cols int32 [num_rows]; out_idx int32 [num_rows][k].
  * num_rows >= 0, row_stride >= 1, 1 <= k <= 2048.
- * The kernel is launched with programmatic stream serialisation and reads
- * visible_cols before it waits for the kernel before it in the stream (the
- * logits after): visible_cols must not be written by that kernel.  The
- * library's scoring kernels never write it.
+ * visible_cols is read before the kernel waits for the kernel before it in
+ * the stream, the logits after (see the conventions above).
  */
 qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
                            const int32_t* visible_cols, int32_t k, int32_t* out_idx,

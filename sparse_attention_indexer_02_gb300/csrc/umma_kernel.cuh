@@ -15,7 +15,10 @@
 //    each row group (tiles past the group's widest visible column are never
 //    scheduled - the early exit of vLLM #62589 "Overview") and takes an equal
 //    contiguous share of the flattened (group, tile) list, plus an equal share
-//    of the pure -inf tail (columns past each group's last tile).
+//    of the pure -inf tail (columns past each group's last tile).  Up to 256
+//    rows, warp 0 builds the schedule and loads its first block-table entries
+//    while the previous kernel in the stream is still running (programmatic
+//    dependent launch); keys, q and weights are read after it completes.
 //  * warp 0 (TMA): per tile, lanes fetch the block-table entries of the tile's
 //    pages and each issues the page's two 64-column K-halves as 3-D tensor
 //    copies into a 128-byte-swizzled stage (aiter #4221 KVBlockSize>=1 commit:
@@ -458,8 +461,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
   }
   // Warm L2 with the visible counts and the block table (a share of their
   // 128-byte lines per CTA, at most kPrefetchLines in all) while the previous
-  // kernel finishes: a prefetch returns no data, so running ahead of that
-  // kernel's writes cannot be observed, and every load below comes after the wait.
+  // kernel finishes.
   if (warp >= 2) {
     const int64_t vis_lines = ((int64_t)p.num_rows * 4 + 127) / 128;
     const int64_t bt_bytes = (int64_t)(p.num_rows / p.rows_per_req) * p.max_pages * 4;
@@ -471,10 +473,16 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
       asm volatile("prefetch.global.L2 [%0];" ::"l"(a));
     }
   }
-  // Everything above overlaps the previous kernel in the stream; no global
-  // memory is loaded before it has completed.
-  ptx::grid_dep_wait();
-  ptx::grid_dep_launch();
+  // Everything above overlaps the previous kernel in the stream.  Few rows:
+  // warp 0 also loads the visible counts (and next_n_lens), builds the
+  // schedule and loads its first block-table entries before it waits for that
+  // kernel - none of the three may be written by it - and every other load,
+  // and every store, comes after the wait.  Many rows: nothing is loaded
+  // before the wait.
+  if (!fast) {
+    ptx::grid_dep_wait();
+    ptx::grid_dep_launch();
+  }
   int32_t vfast[kFastSchedRows / 32], nfast[kFastSchedRows / 32];
   if (fast && warp == 0) {
     // in-range address in every lane; rows past num_rows are masked at use, so
@@ -515,6 +523,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
       // warp 0 arrives on `setup` once its first copies are issued (below):
       // until then the other warps stay parked and leave it the issue slots
     } else {
+      ptx::grid_dep_wait();
+      ptx::grid_dep_launch();
       if (warp == 1) {
         ptx::tmem_alloc(tmem_slot, (uint32_t)L.tmem_cols);
         ptx::tmem_relinquish();
@@ -556,8 +566,11 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     __syncthreads();
   }
   const int total = setup_ok ? pref[G] : 0;
-  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
-  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  // equal shares, the first total % gridDim.x CTAs one tile more: they are
+  // the first to be placed on SMs that the previous kernel has left
+  const int t_share = total / (int)gridDim.x, t_extra = total % (int)gridDim.x;
+  const int t_begin = (int)blockIdx.x * t_share + min((int)blockIdx.x, t_extra);
+  const int t_end = t_begin + t_share + ((int)blockIdx.x < t_extra ? 1 : 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -600,6 +613,10 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     bool released = !fast;  // fast schedule: `setup` not yet arrived on by this warp
     const int32_t* cur_e = t_begin < t_end ? lane_entry(t_begin) : nullptr;
     int32_t cur = load_entry(cur_e);
+    if (fast) {  // the first table entries are in flight; keys and q only after the wait
+      ptx::grid_dep_wait();
+      ptx::grid_dep_launch();
+    }
     for (int tb = t_begin; tb < t_end && ok; tb += tiles_per_batch) {
       // the next batch's block-table entries load while this batch is issued
       const int32_t* nxt_e = lane_entry(tb + tiles_per_batch);
