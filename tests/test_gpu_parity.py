@@ -207,6 +207,55 @@ def test_cuda_graph_capture_and_replay(oracle_mod):
     assert_topk_strict(idx.cpu().numpy(), oracle_mod.select_topk(got, new_vis, s.k))
 
 
+PRECEDED = [SMALL[1], SMALL[3], SMALL[14]]
+
+
+@pytest.mark.parametrize("form", ["two-call", "one-call"])
+@pytest.mark.parametrize("case", PRECEDED + [None], ids=[c[0] for c in PRECEDED] + ["single_row_decode_full"])
+def test_inputs_written_by_the_kernel_just_before(oracle_mod, case, form):
+    """The scoring kernel may start while the kernel before it in the stream is
+    still running and loads q, weights and keys only after that kernel has
+    completed: values written by the kernels just before the call (here q * -2,
+    weights * 0.5, then every key negated, the largest write last) are the ones
+    scored, and the selection right after reads the logits just written.  The
+    row metadata (visible counts, block table) is not written there, as the
+    header's contract asks."""
+    spec = qi.single_row_decode() if case is None else small_spec(case, qi.KV_BF16)
+    inp = qi.build_inputs(spec)
+    d = qi.device_tensors(inp)
+    s = inp.spec
+    stride = d["kv"].shape[1]
+    sign = torch.zeros(stride, dtype=torch.uint8, device="cuda")
+    sign[1::2] = 0x80  # high byte of every little-endian bf16 key element
+
+    def one_call():
+        return torch_api.paged_mqa_topk(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"], s.k,
+                                        page_cols=s.page_cols, out_cols=s.out_cols,
+                                        max_visible=int(s.visible.max()))
+
+    if form == "one-call":
+        one_call()  # its workspace is allocated (and zero-filled) here, not just before the call
+    torch.cuda.synchronize()
+    torch.mul(d["q"], -2.0, out=d["q"])
+    torch.mul(d["weights"], 0.5, out=d["weights"])
+    torch.bitwise_xor(d["kv"], sign, out=d["kv"])
+    if form == "two-call":
+        out = torch.empty((s.num_rows, s.out_cols), dtype=torch.float32, device="cuda")
+        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                   page_cols=s.page_cols, out_cols=s.out_cols, out=out)
+        idx = torch_api.select_topk(out, d["visible"], s.k)
+    else:
+        out, idx = one_call()
+    torch.cuda.synchronize()
+    q_new = qi._bf16_bits((inp.q.astype(np.uint32) << 16).view(np.float32) * np.float32(-2.0))
+    kv_new = inp.kv.copy()
+    kv_new[:, 1::2] ^= np.uint8(0x80)
+    ref = oracle_mod.paged_mqa_logits(inp, q=q_new, weights=inp.weights * np.float32(0.5), kv=kv_new)
+    got = out.cpu().numpy()
+    assert_logits_match(got, ref, qi.KV_BF16, where=f"{s.name} {form}")
+    assert_topk_strict(idx.cpu().numpy(), oracle_mod.select_topk(got, s.visible, s.k), where=f"{s.name} {form}")
+
+
 # --------------------------------------------------------------------------
 # fp8 q x fp8 keys (qsa_paged_mqa_logits_ex)
 # --------------------------------------------------------------------------
