@@ -318,30 +318,48 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
     cluster_wait();
     cluster_sum<NT>(h0, acc, h0, kBins, C);
   }
+  // After each digit: when the bin holding the k-th largest key holds exactly
+  // the keys still wanted, all of them are selected - the selection is every
+  // key at or above the bin's lowest key - and no further digit is needed
+  // (after 22 bits, the usual case).  The test reads the (cluster-summed)
+  // histogram, so every thread and every CTA of a cluster takes the same
+  // branch.  thr is then the bin's lowest key minus one (bins 0 excluded) and
+  // no key equal to it is taken.
   int remaining = k;
   find_digit<NT>(sh, h0, kBins, remaining);
   bar_sync<NT>();
   const uint32_t d0 = (uint32_t)sh.digit;
   remaining -= sh.above;
+  uint32_t thr;
+  if (sh.equal == remaining && d0 != 0u) {
+    thr = (d0 << 21) - 1u;
+    remaining = 0;
+  } else {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j)
-    if (j < mine && (key[j] >> 21) == d0) atomicAdd(&h1[(key[j] >> 10) & 2047u], 1u);
-  bar_sync<NT>();  // every thread has read sh for d0; h1 complete
-  if (multi) cluster_sum<NT>(h1, acc + kBins, h1, kBins, C);
-  find_digit<NT>(sh, h1, kBins, remaining);
-  bar_sync<NT>();
-  const uint32_t p22 = (d0 << 11) | (uint32_t)sh.digit;
-  remaining -= sh.above;
+    for (int j = 0; j < KPT; ++j)
+      if (j < mine && (key[j] >> 21) == d0) atomicAdd(&h1[(key[j] >> 10) & 2047u], 1u);
+    bar_sync<NT>();  // every thread has read sh for d0; h1 complete
+    if (multi) cluster_sum<NT>(h1, acc + kBins, h1, kBins, C);
+    find_digit<NT>(sh, h1, kBins, remaining);
+    bar_sync<NT>();
+    const uint32_t p22 = (d0 << 11) | (uint32_t)sh.digit;
+    remaining -= sh.above;
+    if (sh.equal == remaining && p22 != 0u) {
+      thr = (p22 << 10) - 1u;
+      remaining = 0;
+    } else {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j)
-    if (j < mine && (key[j] >> 10) == p22) atomicAdd(&h2[key[j] & 1023u], 1u);
-  bar_sync<NT>();
-  if (multi) cluster_sum<NT>(h2, acc + 2 * kBins, h2, 1024, C);
-  find_digit<NT>(sh, h2, 1024, remaining);
-  bar_sync<NT>();
-  // the k-th largest key; of the keys equal to it the `remaining` lowest columns are kept
-  const uint32_t thr = (p22 << 10) | (uint32_t)sh.digit;
-  remaining -= sh.above;
+      for (int j = 0; j < KPT; ++j)
+        if (j < mine && (key[j] >> 10) == p22) atomicAdd(&h2[key[j] & 1023u], 1u);
+      bar_sync<NT>();
+      if (multi) cluster_sum<NT>(h2, acc + 2 * kBins, h2, 1024, C);
+      find_digit<NT>(sh, h2, 1024, remaining);
+      bar_sync<NT>();
+      // the k-th largest key; of the keys equal to it the `remaining` lowest columns are kept
+      thr = (p22 << 10) | (uint32_t)sh.digit;
+      remaining -= sh.above;
+    }
+  }
   int gt = 0, eq = 0;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
