@@ -504,6 +504,30 @@ def test_topk_threshold_ties_take_the_lowest_columns(oracle_mod):
     assert_topk_strict(idx, oracle_mod.select_topk(x, vis, 1500))
 
 
+@pytest.mark.parametrize("n", [4096, 8192, 32768])
+def test_topk_threshold_bin_taken_whole(oracle_mod, n):
+    """Row 0: exactly k keys fall in one first-digit bin ([1, 1.25): sign, exponent
+    and two mantissa bits), every other key is lower, and one of them is the float
+    just below 1.0 (the bin's lowest key minus one): the selection may stop after
+    the first digit and must take exactly the bin.  Row 1: the bin holds one key
+    more than wanted, so the later digits decide."""
+    k = 2048
+    rng = np.random.default_rng(n)
+    x = np.empty((2, n), np.float32)
+    below = np.nextafter(np.float32(1.0), np.float32(0.0))
+    top = np.nextafter(np.float32(1.25), np.float32(0.0))
+    for r in range(2):
+        hi = k + r
+        vals = np.concatenate([np.minimum(rng.uniform(1.0, 1.25, hi).astype(np.float32), top),
+                               rng.uniform(0.25, 0.3, n - hi).astype(np.float32)])
+        vals[hi] = below
+        x[r] = vals[rng.permutation(n)]
+    vis = np.array([n, n], np.int32)
+    idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+    assert sorted(idx[0].tolist()) == np.flatnonzero(x[0] >= 1.0).tolist()
+
+
 def test_topk_visible_beyond_stride_is_clamped():
     x = np.arange(40, dtype=np.float32).reshape(2, 20)
     xt = torch.from_numpy(x).cuda()
