@@ -159,6 +159,7 @@ def source_sha(paths):
 
 KERNEL_SOURCES = {
     "rowcore": ["sparse_attention_indexer_02_gb300/csrc/rowcore.cu"],
+    "umma_lean": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
     "umma": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
     "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu", "sparse_attention_indexer_02_gb300/csrc/topk_select.cuh"],
     "umma+topk": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu",
@@ -377,7 +378,8 @@ def run_gpu(args):
     qbuild.build()
     qsa.load_library()
     if args.variant != "auto":
-        qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA}[args.variant])
+        qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA,
+                           "lean": qsa.VARIANT_UMMA_LEAN}[args.variant])
 
     base = qi.WORKLOADS[args.workload]()
     spec = dataclasses.replace(base, seed=base.seed + 7919 * rank)  # per-rank data, same shape
@@ -612,7 +614,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(qi.WORKLOADS), default=DEFAULT_WORKLOAD)
-    ap.add_argument("--variant", choices=["auto", "rowcore", "umma"], default="auto")
+    ap.add_argument("--variant", choices=["auto", "rowcore", "umma", "lean"], default="auto")
     ap.add_argument("--step", choices=["two-call", "fused"], default="two-call",
                     help="time the step as qsa_paged_mqa_logits + qsa_select_topk, or as one qsa_paged_mqa_topk")
     ap.add_argument("--no-rotate", action="store_true")

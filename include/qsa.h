@@ -74,8 +74,12 @@ typedef enum qsa_variant {
   QSA_VARIANT_AUTO = -1,
   QSA_VARIANT_ROWCORE = 0, /* CUDA-core scorer, one row at a time; any shape */
   QSA_VARIANT_UMMA = 1,    /* tcgen05 scorer: 128 keys in M, a request's rows x heads in N */
-  QSA_VARIANT_UMMA_TOPK = 2 /* tcgen05 scorer with the selection in the same kernel
+  QSA_VARIANT_UMMA_TOPK = 2, /* tcgen05 scorer with the selection in the same kernel
                                (qsa_paged_mqa_topk; reported by qsa_last_variant only) */
+  QSA_VARIANT_UMMA_LEAN = 3 /* tcgen05 scorer in its lean form: 8 warps and half an SM's
+                               shared memory, so that a call's CTAs share the SMs with the
+                               kernel before it; groups of at most 64 rows x heads, at most
+                               256 rows, bf16 keys or fp8 keys with fp8 q */
 } qsa_variant;
 
 /* Shape of one qsa_paged_mqa_logits call.  All sizes are host values. */
@@ -247,22 +251,37 @@ qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* byte
  * counter array in place of the caller's workspace.  The pages have no
  * counterpart: it exists for callers that want the fused call without owning
  * device memory for it.  It allocates nothing: the counters are a static
- * device array of 257 words (row groups of at most 128; qsa_paged_mqa_topk_workspace
- * > 1028 bytes is rejected with QSA_ERR_UNSUPPORTED before anything is
- * enqueued).  The array must read zero when a call starts: it is zero when the
- * library is loaded, and every call that completes leaves it zero (a call
- * that set qsa_device_status bit 0 may not).  The first call on each device
- * looks the array's address up (with that device current) and must come
- * before any stream capture on that device.  Calls that may overlap (other
- * streams or host threads) share the one array and race: give each of them
- * qsa_paged_mqa_topk with its own workspace instead.  Arguments, results and
- * the other errors as qsa_paged_mqa_topk.
+ * device array of 257 words, enough for 128 row groups.  A call that would
+ * select inside the scoring kernel over more groups is rejected with
+ * QSA_ERR_UNSUPPORTED before anything is enqueued; calls that take the
+ * scoring and top-k launches instead (more than 256 rows, rows longer than
+ * 16384 columns, the CUDA-core scorer's shapes) never touch the array and
+ * take any number of groups.  The array must read zero when a call starts: it
+ * is zero when the library is loaded, and every call that completes leaves it
+ * zero.  A call that set qsa_device_status bit 0 may not:
+ * qsa_device_status(flags, 1) then zeroes the array as well as the fault word,
+ * or the caller zeroes it in stream order (a cudaMemsetAsync of the address
+ * and size qsa_paged_mqa_topk_noalloc_counters gives).  The first call on each
+ * device looks the array's address up (with that device current) and must
+ * come before any stream capture on that device; the address is kept for the
+ * life of the process, so cudaDeviceReset while the library is loaded is not
+ * supported.  Calls that may overlap (other streams or host threads) share the
+ * one array and race: give each of them qsa_paged_mqa_topk with its own
+ * workspace instead.  Arguments, results and the other errors as
+ * qsa_paged_mqa_topk.
  */
 qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* desc, int32_t q_dtype, const void* q,
                                       const float* weights, const void* kv_cache, const float* scales,
                                       const int32_t* block_table, const int32_t* visible_cols,
                                       const int32_t* next_n_lens, int32_t k, int64_t max_visible,
                                       float* out_logits, int32_t* out_idx, void* stream);
+
+/* Device address (*device_ptr) and size in bytes (*bytes) of the counter array
+ * of qsa_paged_mqa_topk_noalloc on the current device, looked up as that
+ * call's first use on the device does (so not during a stream capture).  For
+ * callers that zero the array in stream order after a call that set
+ * qsa_device_status bit 0; nothing else may write it. */
+qsa_status qsa_paged_mqa_topk_noalloc_counters(void** device_ptr, size_t* bytes);
 
 /*
  * qsa_plan_variant - host-only dispatch decision for `desc` (no CUDA call).
@@ -271,11 +290,19 @@ qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* desc, int32_t q_dtyp
  * device sync, as vLLM #62589 "Dispatch" does for its one-row kernel.  On
  * GB300 the tcgen05 scorer measures faster than the CUDA-core one-row scorer
  * at every row count (single-row decode included), so shapes it supports go
- * to it; everything else (head counts other than 1, 2, 4, ..., 64, page sizes
- * that are not a multiple of 8 dividing 128 or a multiple of 128, misaligned
- * fp8 scales) goes to the CUDA-core scorer.
+ * to it - its lean form for decode-sized calls (at most 256 rows, groups of
+ * at most 64 rows x heads, three 32 KB key stages in its shared memory), its
+ * full form otherwise; everything else (head counts other than 1, 2, 4, ...,
+ * 64, page sizes that are not a multiple of 8 dividing 128 or a multiple of
+ * 128, misaligned fp8 scales) goes to the CUDA-core scorer.
  */
 qsa_status qsa_plan_variant(const qsa_paged_desc* desc, int32_t* variant);
+
+/* qsa_plan_variant for q of element type q_dtype (qsa_q_dtype), as
+ * qsa_paged_mqa_logits_ex with that q_dtype would choose: fp8 keys with fp8 q
+ * may take the lean tcgen05 form, fp8 keys with bf16 q never do (their keys
+ * are widened by the converter warps of the full form). */
+qsa_status qsa_plan_variant_ex(const qsa_paged_desc* desc, int32_t q_dtype, int32_t* variant);
 
 /* Force a variant for later calls (QSA_VARIANT_AUTO restores the dispatch).
  * A forced variant that cannot serve a shape makes the call return
@@ -295,8 +322,11 @@ const char* qsa_last_error(void);
  * scoring kernel gave up waiting on one of its internal barriers (about one
  * second): that launch left its output incomplete and returned early instead
  * of hanging the GPU.  Bit 1: a top-k launch gave up waiting for its row copy
- * (its selection for that row is unspecified).  Synchronises the current device, then writes the word
- * to *flags (host pointer) and clears it when `clear` is non-zero.
+ * (its selection for that row is unspecified).  Synchronises the current
+ * device, then writes the word to *flags (host pointer).  When `clear` is
+ * non-zero it then clears the word and zeroes the counter array of
+ * qsa_paged_mqa_topk_noalloc on the current device (synchronously), so the
+ * next no-alloc call starts clean after a failed one.
  */
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear);
 

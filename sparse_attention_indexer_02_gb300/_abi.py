@@ -17,12 +17,15 @@ LIB_PATH = os.path.join(_PKG, "libqsa.so")
 QSA_OK, QSA_ERR_INVALID_ARG, QSA_ERR_UNSUPPORTED, QSA_ERR_CUDA = 0, 1, 2, 3
 KV_BF16, KV_FP8_E4M3 = 0, 1
 Q_BF16, Q_FP8_E4M3 = 0, 1
-VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA, VARIANT_UMMA_TOPK = -1, 0, 1, 2
-VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma", VARIANT_UMMA_TOPK: "umma+topk"}
+VARIANT_AUTO, VARIANT_ROWCORE, VARIANT_UMMA, VARIANT_UMMA_TOPK, VARIANT_UMMA_LEAN = -1, 0, 1, 2, 3
+VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma", VARIANT_UMMA_TOPK: "umma+topk",
+                 VARIANT_UMMA_LEAN: "umma_lean"}
 
 # Every symbol include/qsa.h declares.
 EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_paged_mqa_topk",
-            "qsa_paged_mqa_topk_workspace", "qsa_paged_mqa_topk_noalloc", "qsa_select_topk", "qsa_plan_variant", "qsa_force_variant",
+            "qsa_paged_mqa_topk_workspace", "qsa_paged_mqa_topk_noalloc",
+            "qsa_paged_mqa_topk_noalloc_counters", "qsa_select_topk", "qsa_plan_variant",
+            "qsa_plan_variant_ex", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
 
 
@@ -76,6 +79,8 @@ def load_library():
         lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
         lib.qsa_plan_variant.restype = ctypes.c_int
         lib.qsa_plan_variant.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(i32)]
+        lib.qsa_plan_variant_ex.restype = ctypes.c_int
+        lib.qsa_plan_variant_ex.argtypes = [ctypes.POINTER(PagedDesc), i32, ctypes.POINTER(i32)]
         lib.qsa_force_variant.restype = None
         lib.qsa_force_variant.argtypes = [i32]
         lib.qsa_last_variant.restype = i32
@@ -86,6 +91,9 @@ def load_library():
         lib.qsa_last_error.argtypes = []
         lib.qsa_abi_version.restype = i32
         lib.qsa_abi_version.argtypes = []
+        lib.qsa_paged_mqa_topk_noalloc_counters.restype = ctypes.c_int
+        lib.qsa_paged_mqa_topk_noalloc_counters.argtypes = [ctypes.POINTER(ctypes.c_void_p),
+                                                            ctypes.POINTER(ctypes.c_size_t)]
         lib.qsa_device_status.restype = ctypes.c_int
         lib.qsa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         _lib = lib
@@ -186,9 +194,12 @@ def select_topk(logits, num_rows: int, row_stride: int, visible_cols, k: int, ou
     _check(st)
 
 
-def plan_variant(desc: PagedDesc) -> int:
+def plan_variant(desc: PagedDesc, q_dtype: int | None = None) -> int:
     v = ctypes.c_int32(-1)
-    _check(load_library().qsa_plan_variant(ctypes.byref(desc), ctypes.byref(v)))
+    if q_dtype is None:
+        _check(load_library().qsa_plan_variant(ctypes.byref(desc), ctypes.byref(v)))
+    else:
+        _check(load_library().qsa_plan_variant_ex(ctypes.byref(desc), int(q_dtype), ctypes.byref(v)))
     return v.value
 
 
@@ -198,6 +209,14 @@ def force_variant(v: int) -> None:
 
 def last_variant() -> int:
     return load_library().qsa_last_variant()
+
+
+def noalloc_counters() -> tuple[int, int]:
+    """(device address, bytes) of qsa_paged_mqa_topk_noalloc's counter array on
+    the current device."""
+    ptr, n = ctypes.c_void_p(0), ctypes.c_size_t(0)
+    _check(load_library().qsa_paged_mqa_topk_noalloc_counters(ctypes.byref(ptr), ctypes.byref(n)))
+    return int(ptr.value or 0), int(n.value)
 
 
 def device_status(clear: bool = True) -> int:

@@ -102,7 +102,12 @@ void qsa_force_variant(int32_t v) { g_forced_variant.store(v); }
 
 int32_t qsa_last_variant(void) { return g_last_variant; }
 
-qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) {
+}  // extern "C"
+
+namespace {
+
+// Variant for `d` with q of type q8 (fp8) or bf16; see qsa_plan_variant.
+qsa_status plan(const qsa_paged_desc* d, bool q8, int32_t* variant) {
   qsa_status st = validate_desc(d);
   if (st != QSA_OK) return st;
   if (!variant) return fail(QSA_ERR_INVALID_ARG, "variant is NULL");
@@ -114,6 +119,14 @@ qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) {
     if (!qsa::umma_supports(*d, &why))
       return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant cannot serve this shape: %s", why);
     *variant = QSA_VARIANT_UMMA;
+  } else if (forced == QSA_VARIANT_UMMA_LEAN) {
+    if (!qsa::umma_lean_supports(*d, q8, &why))
+      return fail(QSA_ERR_UNSUPPORTED, "forced lean tcgen05 variant cannot serve this shape: %s", why);
+    *variant = QSA_VARIANT_UMMA_LEAN;
+  } else if (qsa::umma_lean_supports(*d, q8, &why)) {
+    // decode-sized calls: the lean form, whose CTAs share the SMs with the
+    // kernel before it and stream their first keys while it finishes
+    *variant = QSA_VARIANT_UMMA_LEAN;
   } else if (qsa::umma_supports(*d, &why)) {
     // Measured on GB300: the tcgen05 scorer is faster than the CUDA-core
     // one-row scorer at every row count, single-row decode included (its
@@ -124,6 +137,20 @@ qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) {
     *variant = QSA_VARIANT_ROWCORE;
   }
   return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_plan_variant(const qsa_paged_desc* d, int32_t* variant) { return plan(d, false, variant); }
+
+qsa_status qsa_plan_variant_ex(const qsa_paged_desc* d, int32_t q_dtype, int32_t* variant) {
+  if (q_dtype != QSA_Q_BF16 && q_dtype != QSA_Q_FP8_E4M3)
+    return fail(QSA_ERR_INVALID_ARG, "q_dtype must be QSA_Q_BF16 or QSA_Q_FP8_E4M3 (got %d)", q_dtype);
+  if (d && q_dtype == QSA_Q_FP8_E4M3 && d->kv_dtype != QSA_KV_FP8_E4M3)
+    return fail(QSA_ERR_INVALID_ARG, "fp8 q needs fp8 keys (mixed operand types)");
+  return plan(d, q_dtype == QSA_Q_FP8_E4M3, variant);
 }
 
 qsa_status qsa_paged_mqa_logits(const qsa_paged_desc* d, const void* q, const float* weights,
@@ -172,11 +199,11 @@ qsa_status prepare_scoring(const qsa_paged_desc* d, int32_t q_dtype, const void*
       !aligned(out_logits, 4) || (fp8 && !aligned(scales, 4)) || !aligned(next_n_lens, 4))
     return fail(QSA_ERR_INVALID_ARG,
                 "weights, block_table, visible_cols, next_n_lens, out_logits, scales must be 4-byte aligned");
-  st = qsa_plan_variant(d, variant);
+  st = plan(d, q8, variant);
   if (st != QSA_OK) return st;
   // the tcgen05 scorer bulk-copies fp8 scales, which needs a 16-byte aligned base
-  if (*variant == QSA_VARIANT_UMMA && fp8 && !aligned(scales, 16)) {
-    if (g_forced_variant.load() == QSA_VARIANT_UMMA)
+  if ((*variant == QSA_VARIANT_UMMA || *variant == QSA_VARIANT_UMMA_LEAN) && fp8 && !aligned(scales, 16)) {
+    if (g_forced_variant.load() != QSA_VARIANT_AUTO)
       return fail(QSA_ERR_UNSUPPORTED, "forced tcgen05 variant needs 16-byte aligned fp8 scales");
     *variant = QSA_VARIANT_ROWCORE;
   }
@@ -208,8 +235,9 @@ qsa_status prepare_scoring(const qsa_paged_desc* d, int32_t q_dtype, const void*
 qsa_status launch_scoring(const qsa::ScoreParams& p, int32_t variant, cudaStream_t s,
                           const qsa::FuseArgs* fuse) {
   const char* msg = "launch failed";
-  cudaError_t e = variant == QSA_VARIANT_UMMA ? qsa::launch_umma(p, s, &msg, fuse)
-                                              : qsa::launch_rowcore(p, s, &msg);
+  cudaError_t e = variant == QSA_VARIANT_ROWCORE
+                      ? qsa::launch_rowcore(p, s, &msg)
+                      : qsa::launch_umma(p, s, &msg, fuse, variant == QSA_VARIANT_UMMA_LEAN);
   if (e == cudaErrorInvalidValue && msg && strcmp(msg, "launch failed") != 0)
     return fail(QSA_ERR_UNSUPPORTED, "%s", msg);
   if (e != cudaSuccess)
@@ -260,6 +288,66 @@ cudaError_t noalloc_counters(uint32_t** out) {
   return cudaSuccess;
 }
 
+// qsa_paged_mqa_topk (workspace given) and qsa_paged_mqa_topk_noalloc (the
+// library's counter array, looked up only when the fused selection runs).
+qsa_status topk_call(const qsa_paged_desc* d, int32_t q_dtype, const void* q, const float* weights,
+                     const void* kv_cache, const float* scales, const int32_t* block_table,
+                     const int32_t* visible_cols, const int32_t* next_n_lens, int32_t k, int64_t max_visible,
+                     float* out_logits, int32_t* out_idx, void* workspace, size_t workspace_bytes, bool noalloc,
+                     void* stream) {
+  qsa::ScoreParams p;
+  int32_t variant = 0;
+  bool empty = false;
+  qsa_status st = prepare_scoring(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols,
+                                  next_n_lens, out_logits, &p, &variant, &empty);
+  if (st != QSA_OK) return st;
+  if (k < 1 || k > 2048) return fail(QSA_ERR_INVALID_ARG, "k must be in 1..2048 (got %d)", k);
+  if (empty) {
+    g_last_variant = -1;
+    if ((int64_t)d->num_requests * d->rows_per_req == 0) return QSA_OK;
+    // rows but no column: every row selects nothing
+    if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be 4-byte aligned");
+    const size_t n = (size_t)d->num_requests * d->rows_per_req * k * sizeof(int32_t);
+    cudaError_t e = cudaMemsetAsync(out_idx, 0xFF, n, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "filling out_idx: %s", cudaGetErrorString(e));
+    return QSA_OK;
+  }
+  if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be non-NULL, 4-byte aligned");
+  const int64_t words = fused_words(d);
+  if (!noalloc && words > 0 && (!workspace || !aligned(workspace, 4) || workspace_bytes < (size_t)words * 4))
+    return fail(QSA_ERR_INVALID_ARG, "workspace must be 4-byte aligned and hold %lld bytes", (long long)words * 4);
+  const int64_t bound = max_visible > 0 && max_visible < p.capacity ? max_visible : p.capacity;
+  // the fused selection runs in the full form of the tcgen05 scorer (the lean
+  // form is taken for the scoring alone unless it was forced)
+  const bool tc = variant == QSA_VARIANT_UMMA ||
+                  (variant == QSA_VARIANT_UMMA_LEAN && g_forced_variant.load() == QSA_VARIANT_AUTO);
+  const bool fused = tc && words > 0 && p.num_rows <= kFuseMaxRows && bound <= kFuseMaxVisible;
+  if (fused && noalloc) {
+    if (words > kNoAllocWords)
+      return fail(QSA_ERR_UNSUPPORTED,
+                  "qsa_paged_mqa_topk_noalloc holds counters for %d row groups and this call selects in the "
+                  "scoring kernel over %lld: call qsa_paged_mqa_topk with a workspace of %lld bytes",
+                  kNoAllocGroups, (long long)(words - 1) / 2, (long long)words * 4);
+    uint32_t* counters = nullptr;
+    cudaError_t e = noalloc_counters(&counters);
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "counter address: %s", cudaGetErrorString(e));
+    workspace = counters;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fused) {
+    const qsa::FuseArgs fa{out_idx, static_cast<uint32_t*>(workspace), k};
+    st = launch_scoring(p, QSA_VARIANT_UMMA, s, &fa);
+    if (st == QSA_OK) g_last_variant = QSA_VARIANT_UMMA_TOPK;
+    return st;
+  }
+  st = launch_scoring(p, variant, s, nullptr);
+  if (st != QSA_OK) return st;
+  cudaError_t e = qsa::launch_topk(out_logits, p.num_rows, p.out_cols, visible_cols, next_n_lens, p.rows_per_req,
+                                   p.capacity, k, out_idx, s);
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
+  return QSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -294,43 +382,8 @@ qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* d, int32_t q_dtype, const vo
                               const int32_t* visible_cols, const int32_t* next_n_lens, int32_t k,
                               int64_t max_visible, float* out_logits, int32_t* out_idx, void* workspace,
                               size_t workspace_bytes, void* stream) {
-  qsa::ScoreParams p;
-  int32_t variant = 0;
-  bool empty = false;
-  qsa_status st = prepare_scoring(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols,
-                                  next_n_lens, out_logits, &p, &variant, &empty);
-  if (st != QSA_OK) return st;
-  if (k < 1 || k > 2048) return fail(QSA_ERR_INVALID_ARG, "k must be in 1..2048 (got %d)", k);
-  if (empty) {
-    g_last_variant = -1;
-    if ((int64_t)d->num_requests * d->rows_per_req == 0) return QSA_OK;
-    // rows but no column: every row selects nothing
-    if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be 4-byte aligned");
-    const size_t n = (size_t)d->num_requests * d->rows_per_req * k * sizeof(int32_t);
-    cudaError_t e = cudaMemsetAsync(out_idx, 0xFF, n, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "filling out_idx: %s", cudaGetErrorString(e));
-    return QSA_OK;
-  }
-  if (!out_idx || !aligned(out_idx, 4)) return fail(QSA_ERR_INVALID_ARG, "out_idx must be non-NULL, 4-byte aligned");
-  const int64_t words = fused_words(d);
-  if (words > 0 && (!workspace || !aligned(workspace, 4) || workspace_bytes < (size_t)words * 4))
-    return fail(QSA_ERR_INVALID_ARG, "workspace must be 4-byte aligned and hold %lld bytes", (long long)words * 4);
-  const int64_t bound = max_visible > 0 && max_visible < p.capacity ? max_visible : p.capacity;
-  const bool fused =
-      variant == QSA_VARIANT_UMMA && words > 0 && p.num_rows <= kFuseMaxRows && bound <= kFuseMaxVisible;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fused) {
-    const qsa::FuseArgs fa{out_idx, static_cast<uint32_t*>(workspace), k};
-    st = launch_scoring(p, variant, s, &fa);
-    if (st == QSA_OK) g_last_variant = QSA_VARIANT_UMMA_TOPK;
-    return st;
-  }
-  st = launch_scoring(p, variant, s, nullptr);
-  if (st != QSA_OK) return st;
-  cudaError_t e = qsa::launch_topk(out_logits, p.num_rows, p.out_cols, visible_cols, next_n_lens, p.rows_per_req,
-                                   p.capacity, k, out_idx, s);
-  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
-  return QSA_OK;
+  return topk_call(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols, next_n_lens, k, max_visible,
+                   out_logits, out_idx, workspace, workspace_bytes, false, stream);
 }
 
 qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* d, int32_t q_dtype, const void* q,
@@ -338,28 +391,33 @@ qsa_status qsa_paged_mqa_topk_noalloc(const qsa_paged_desc* d, int32_t q_dtype, 
                                       const int32_t* block_table, const int32_t* visible_cols,
                                       const int32_t* next_n_lens, int32_t k, int64_t max_visible,
                                       float* out_logits, int32_t* out_idx, void* stream) {
-  qsa_status st = validate_desc(d);
-  if (st != QSA_OK) return st;
-  const int64_t words = fused_words(d);
-  if (words > kNoAllocWords)
-    return fail(QSA_ERR_UNSUPPORTED,
-                "qsa_paged_mqa_topk_noalloc holds counters for %d row groups and this shape has %lld: "
-                "call qsa_paged_mqa_topk with a workspace of %lld bytes",
-                kNoAllocGroups, (long long)(words - 1) / 2, (long long)words * 4);
+  return topk_call(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols, next_n_lens, k, max_visible,
+                   out_logits, out_idx, nullptr, 0, true, stream);
+}
+
+qsa_status qsa_paged_mqa_topk_noalloc_counters(void** device_ptr, size_t* bytes) {
+  if (!device_ptr || !bytes) return fail(QSA_ERR_INVALID_ARG, "device_ptr and bytes must be non-NULL");
   uint32_t* counters = nullptr;
-  if (words > 0) {
-    cudaError_t e = noalloc_counters(&counters);
-    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "counter address: %s", cudaGetErrorString(e));
-  }
-  return qsa_paged_mqa_topk(d, q_dtype, q, weights, kv_cache, scales, block_table, visible_cols, next_n_lens, k,
-                            max_visible, out_logits, out_idx, counters, words > 0 ? sizeof(g_noalloc_counters) : 0,
-                            stream);
+  cudaError_t e = noalloc_counters(&counters);
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "counter address: %s", cudaGetErrorString(e));
+  *device_ptr = counters;
+  *bytes = sizeof(g_noalloc_counters);
+  return QSA_OK;
 }
 
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(QSA_ERR_INVALID_ARG, "flags is NULL");
   cudaError_t e = qsa::read_fault_word(flags, clear != 0);
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "reading the device fault word: %s", cudaGetErrorString(e));
+  if (clear) {
+    // the device is idle (read_fault_word synchronised it): put the no-alloc
+    // call's counters back to zero too, whatever a failed call left there
+    uint32_t* counters = nullptr;
+    e = noalloc_counters(&counters);
+    if (e == cudaSuccess) e = cudaMemset(counters, 0, sizeof(g_noalloc_counters));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "clearing the no-alloc counters: %s", cudaGetErrorString(e));
+  }
   return QSA_OK;
 }
 

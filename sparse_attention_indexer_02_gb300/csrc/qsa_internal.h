@@ -39,10 +39,12 @@ struct FuseArgs {
 // when a shape is rejected (then the return is cudaErrorInvalidValue).
 cudaError_t launch_rowcore(const ScoreParams& p, cudaStream_t stream, const char** msg);
 bool umma_supports(const qsa_paged_desc& d, const char** why);
+// The lean form of the tcgen05 scorer serves `d` (with fp8 q when q8).
+bool umma_lean_supports(const qsa_paged_desc& d, bool q8, const char** why);
 // Row groups the tcgen05 scorer splits `d` into (rows x heads of a group <= 256).
 int64_t umma_num_groups(const qsa_paged_desc& d);
 cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg,
-                        const FuseArgs* fuse = nullptr);
+                        const FuseArgs* fuse = nullptr, bool lean = false);
 // Device address of the fault word on the current device (bit 0: a scoring
 // kernel's bounded wait gave up; bit 1: a top-k kernel's).
 cudaError_t fault_word_address(unsigned int** out);

@@ -77,6 +77,16 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1, int32_t c2,
+                                            int32_t c3, int32_t c4, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
 // Plain (untensored) bulk copy global -> shared; sizes and addresses 16-byte aligned.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
@@ -169,13 +179,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
-// layout: 8-row x 128-byte atoms stacked along M/N every 1024 bytes (SBO);
-// the leading offset is unused for this layout.  Version bits = 1 (sm_100).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr) {
+// layout: 8-row x 128-byte atoms stacked along M/N every `sbo` bytes (1024
+// when they are back to back); the leading offset is unused for this layout.
+// Version bits = 1 (sm_100).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t sbo = 1024u) {
   uint64_t d = 0;
   d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
   d |= (uint64_t)(16u >> 4) << 16;
-  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
   d |= (uint64_t)2 << 61;
   return d;

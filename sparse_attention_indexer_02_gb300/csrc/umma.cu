@@ -112,13 +112,39 @@ bool umma_supports(const qsa_paged_desc& d, const char** why) {
   return true;
 }
 
+bool umma_lean_supports(const qsa_paged_desc& d, bool q8, const char** why) {
+  if (!umma_supports(d, why)) return false;
+  if (d.kv_dtype == QSA_KV_FP8_E4M3 && !q8) {
+    *why = "the lean form has no fp8 -> bf16 converter (fp8 keys need fp8 q)";
+    return false;
+  }
+  if ((int64_t)d.num_requests * d.rows_per_req > kFastSchedRows) {
+    *why = "the lean form serves at most 256 rows";
+    return false;
+  }
+  int Gr, N;
+  group_shape(d, &Gr, &N);
+  const int64_t groups = (int64_t)d.num_requests * ((d.rows_per_req + Gr - 1) / Gr);
+  if (N > kLeanMaxN) {
+    *why = "the lean form serves groups of at most 64 rows x heads";
+    return false;
+  }
+  const int kind = d.kv_dtype == QSA_KV_FP8_E4M3 ? kKindFp8Q : kKindBf16;
+  if (make_layout(N, (int)groups, kind, false, true).stages < 3) {
+    *why = "the lean form's shared memory holds fewer than three key stages";
+    return false;
+  }
+  return true;
+}
+
 int64_t umma_num_groups(const qsa_paged_desc& d) {
   int Gr, N;
   group_shape(d, &Gr, &N);
   return (int64_t)d.num_requests * ((d.rows_per_req + Gr - 1) / Gr);
 }
 
-cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg, const FuseArgs* fuse) {
+cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** msg, const FuseArgs* fuse,
+                        bool lean) {
   if (p.num_rows == 0 || p.out_cols == 0) return cudaSuccess;
   qsa_paged_desc d{};
   d.num_requests = p.num_requests;
@@ -131,6 +157,10 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   d.key_page_stride = p.key_page_stride;
   d.scale_page_stride = p.scale_page_stride;
   if (!umma_supports(d, msg)) return cudaErrorInvalidValue;
+  if (lean && (fuse != nullptr || !umma_lean_supports(d, p.q8 != 0, msg))) {
+    if (fuse != nullptr) *msg = "the lean form has no fused selection";
+    return cudaErrorInvalidValue;
+  }
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (!enc) {
     *msg = "cuTensorMapEncodeTiled is unavailable from the driver";
@@ -172,20 +202,34 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   up.keep_keys = up.groups_per_req > 1 ? 1 : 0;
 
   CUtensorMap kv_map, q_map;
-  {
-    // bf16: two 64-element (128-byte) K-halves per page row; fp8: one 128-byte row
+  CUresult r;
+  if (p.fp8) {
+    // fp8: one 128-byte row (all of D) per key; a box is a page's (or a
+    // 128-key slice of a page's) rows
     cuuint64_t dims[3] = {128, (cuuint64_t)p.page_cols, (cuuint64_t)p.num_pages};
-    cuuint64_t strides[2] = {(cuuint64_t)(p.fp8 ? 128 : 256), (cuuint64_t)p.key_page_stride};
-    cuuint32_t box[3] = {(cuuint32_t)(p.fp8 ? 128 : 64), (cuuint32_t)up.box_rows, 1};
+    cuuint64_t strides[2] = {128, (cuuint64_t)p.key_page_stride};
+    cuuint32_t box[3] = {128, (cuuint32_t)up.box_rows, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(&kv_map, p.fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                     const_cast<uint8_t*>(p.kv), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      *msg = "key-cache tensor map rejected by the driver";
-      return cudaErrorInvalidValue;
-    }
+    r = enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(p.kv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    // bf16: a key row is two 64-element (128-byte) K-halves.  Dimensions,
+    // innermost first: element of the half, key within its group of 8, half,
+    // group of 8 within the page, page.  One box of a page's rows then lands
+    // as, per group of 8 keys, K-half 0 (a 1 KB swizzle atom) then K-half 1 -
+    // a whole page in one copy.
+    cuuint64_t dims[5] = {64, 8, 2, (cuuint64_t)(p.page_cols / 8), (cuuint64_t)p.num_pages};
+    cuuint64_t strides[4] = {256, 128, 8 * 256, (cuuint64_t)p.key_page_stride};
+    cuuint32_t box[5] = {64, 8, 2, (cuuint32_t)(up.box_rows / 8), 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    r = enc(&kv_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<uint8_t*>(p.kv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) {
+    *msg = "key-cache tensor map rejected by the driver";
+    return cudaErrorInvalidValue;
   }
   {
     // bf16 q: 64-element (128-byte) K-halves; fp8 q: one 128-byte row of D codes
@@ -193,7 +237,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
     cuuint64_t strides[1] = {(cuuint64_t)(p.q8 ? 128 : 256)};
     cuuint32_t box[2] = {(cuuint32_t)(p.q8 ? 128 : 64), (cuuint32_t)N};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = enc(&q_map, p.q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    r = enc(&q_map, p.q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                      const_cast<uint16_t*>(p.q), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -208,7 +252,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   const int64_t upper = (int64_t)up.num_groups * up.tiles_cap;
   const int grid = (int)(upper < info.num_sms ? (upper < 1 ? 1 : upper) : info.num_sms);
   const int kind = !p.fp8 ? kKindBf16 : (p.q8 ? kKindFp8Q : kKindFp8Keys);
-  const Layout L = make_layout(N, up.num_groups, kind, fuse != nullptr);
+  const Layout L = make_layout(N, up.num_groups, kind, fuse != nullptr, lean);
   up.topk_out = nullptr;
   up.fuse_sync = nullptr;
   up.topk_k = up.topk_cap = up.topk_cpw = 0;
@@ -237,6 +281,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
     return p.fp8 ? launch_fp8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream)
                  : launch_bf16_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);
   }
+  if (lean) return launch_lean(p.num_heads, kind, kv_map, q_map, up, L, grid, stream);
   if (kind == kKindFp8Q) return launch_q8(p.num_heads, kv_map, q_map, up, L, grid, stream);
   return p.fp8 ? launch_fp8(p.num_heads, kv_map, q_map, up, L, grid, stream)
                : launch_bf16(p.num_heads, kv_map, q_map, up, L, grid, stream);

@@ -53,17 +53,27 @@ constexpr int kKindFp8Q = 2;                // fp8 keys, fp8 q: kind::f8f6f4 MMA
 constexpr int kBM = 128;                    // keys per tile (MMA M)
 constexpr int kHalfBytes = kBM * 128;       // one 64-element K-half of a bf16 key tile
 constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB
+// A bf16 key tile as the copies leave it: for each group of 8 keys, their
+// 64-element K-half 0 (a 1 KB 128-byte-swizzle atom), then their K-half 1, so
+// one copy moves whole keys (both halves of a page's rows) and the MMA reads
+// K-half h of 8-key group i at h * 1024 + i * 2048.
+constexpr uint32_t kBf16AtomStride = 2048;
 constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
 constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
 constexpr int kFp8StageAlloc = kFp8StageBytes + 1024;  // + the block's 128 fp32 scales, 1024-aligned
 constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (see the converter)
 // Warp roles: 0 TMA, 1 MMA, then the epilogue warps (three per TMEM lane
-// quadrant, or one with the fp8 -> bf16 converter), then 8 converter warps
-// (fp8 keys with bf16 q) or 2 spare warps that write the -inf tail (ptxas 13.0
-// for aarch64 hosts crashes on this kernel when no warps follow the epilogue).
-template <bool CONV>
+// quadrant, or one with the fp8 -> bf16 converter or in the lean form), then
+// 8 converter warps (fp8 keys with bf16 q) or 2 spare warps that write the
+// -inf tail (ptxas 13.0 for aarch64 hosts crashes on this kernel when no warps
+// follow the epilogue).  The lean form (8 warps, at most 128 registers a
+// thread and half an SM's shared memory) serves decode-sized groups: two of
+// its CTAs fit an SM, so a call's CTAs are resident, with their schedule built
+// and their first block-table entries loaded, while the kernel before them
+// still runs, and stream keys the moment it completes.
+template <bool CONV, bool LEAN = false>
 struct Roles {
-  static constexpr int kEpiWarps = CONV ? 4 : 12;
+  static constexpr int kEpiWarps = (CONV || LEAN) ? 4 : 12;
   static constexpr int kEpiThreads = 32 * kEpiWarps;
   static constexpr int kConvWarps = CONV ? 8 : 2;
   static constexpr int kConvThreads = 32 * kConvWarps;
@@ -73,6 +83,8 @@ constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kFastSchedRows = 256;              // up to this many rows one warp builds the schedule
 constexpr int64_t kPrefetchLines = 8192;         // block-table lines warmed in L2 before the wait (1 MB)
 constexpr int kMaxSmem = 232448;                 // 227 KB opt-in limit per CTA
+constexpr int kLeanSmem = 115712;                // two CTAs an SM: 2 x (this + 1 KB reserved) <= 228 KB
+constexpr int kLeanMaxN = 64;                    // lean form: groups of at most 64 rows x heads
 // Fused selection: at most kFuseMaxGroups row groups (their counters live in
 // the caller's workspace, the list of groups a CTA completed in shared memory).
 constexpr int kFuseWords = 4 + kFuseMaxGroups;   // won count, claim key, claimed row, last flag; won groups
@@ -116,7 +128,7 @@ struct Layout {
   int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, fuse_off, total;
 };
 
-inline Layout make_layout(int N, int groups, int kind, bool fused = false) {
+inline Layout make_layout(int N, int groups, int kind, bool fused = false, bool lean = false) {
   const bool fp8 = kind != kKindBf16, conv = kind == kKindFp8Keys;
   Layout L;
   L.n = N;
@@ -127,7 +139,7 @@ inline Layout make_layout(int N, int groups, int kind, bool fused = false) {
   const int ring = conv ? kScaleRing * kBM * 4 : 0;
   const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
                    8 * (groups + 1) + (fused ? 16 + 4 * kFuseWords : 0);
-  int st = (kMaxSmem - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
+  int st = ((lean ? kLeanSmem : kMaxSmem) - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;
   L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
   L.b_off = L.a_off + L.a_stages * kTileBytes;
@@ -384,14 +396,15 @@ __device__ __forceinline__ void fused_select(const UmmaParams& p, const int32_t*
   }
 }
 
-template <int H, int KIND, bool FUSE>
-__global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
+template <int H, int KIND, bool FUSE, bool LEAN = false>
+__global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, LEAN ? 2 : 1)
     umma_score_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const UmmaParams p, const Layout L) {
   constexpr bool FP8 = KIND != kKindBf16;      // fp8 keys (+ per-key scales)
   constexpr bool CONV = KIND == kKindFp8Keys;  // widened to bf16 by the converter warps
   constexpr bool Q8 = KIND == kKindFp8Q;       // fp8 q: e4m3 x e4m3 MMA on the copied keys
-  using R = Roles<CONV>;
+  static_assert(!LEAN || (!CONV && !FUSE), "the lean form has no converter and no fused selection");
+  using R = Roles<CONV, LEAN>;
   constexpr int kThreads = R::kThreads;
   constexpr int kEpiThreads = R::kEpiThreads;
   extern __shared__ uint8_t smem_raw[];
@@ -583,8 +596,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
     // columns always; otherwise a 32-bit division)
     auto page_of = [&](int c) { return p.pc_shift >= 0 ? c >> p.pc_shift : c / pc; };
     auto req_of = [&](int g) { return p.groups_per_req == 1 ? g : g / p.groups_per_req; };
-    const uint32_t box_bytes = (uint32_t)p.box_rows * 128u;  // per K-half (bf16) or per page (fp8)
-    const uint32_t copies = FP8 ? 1u : 2u;
+    const uint32_t box_bytes = (uint32_t)p.box_rows * (FP8 ? 128u : 256u);  // one copy per page (box)
     // Block-table entry of this lane's box in the batch starting at tile tb
     // (null: no box).  Lane l covers tile tb + l / bpt, box l % bpt.
     auto lane_entry = [&](int tb) -> const int32_t* {
@@ -648,15 +660,15 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
         ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, p.fault);
         if (!ok) break;
         if (lane == 0)
-          ptx::mbar_arrive_expect_tx(&full[stage], copies * nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
+          ptx::mbar_arrive_expect_tx(&full[stage], nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
         __syncwarp();
         if ((lane >> bsh) == i && cur_e != nullptr) {
           const int32_t pg = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);  // clamp: no fault
           const int box = lane & (bpt - 1);
           const int y = pc >= kBM ? c0 - page_of(c0) * pc : 0;
-          uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * 128u;
-          ptx::tma_load_3d(dst, &kv_map, 0, y, pg, &full[stage], policy);
-          if (!FP8) ptx::tma_load_3d(dst + kHalfBytes, &kv_map, 64, y, pg, &full[stage], policy);
+          uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * (FP8 ? 128u : 256u);
+          if (FP8) ptx::tma_load_3d(dst, &kv_map, 0, y, pg, &full[stage], policy);
+          else ptx::tma_load_5d(dst, &kv_map, 0, 0, 0, y >> 3, pg, &full[stage], policy);
           if (FP8)  // the box's scales land after the key rows of the stage (plain bulk copy:
                     // 16-byte aligned source, destination and size)
             ptx::bulk_load(S + stage * L.stage_bytes + kFp8StageBytes + box * p.box_rows * 4,
@@ -729,7 +741,10 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys>::kThreads, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (uint32_t)(k & 3) * 32u;
-            const uint64_t ad = ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff);
+            // copied bf16 keys: halves interleaved per 8-key group; widened
+            // fp8 keys: one 16 KB block per K-half
+            const uint64_t ad = CONV ? ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff)
+                                     : ptx::sw128_desc(a0 + (k >> 2) * 1024u + koff, kBf16AtomStride);
             const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
             ptx::mma_bf16(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
           }
@@ -979,6 +994,9 @@ cudaError_t launch_fp8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, 
                        const Layout& L, int grid, cudaStream_t s);
 cudaError_t launch_q8(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                       const Layout& L, int grid, cudaStream_t s);
+// The lean form (umma_lean.cu): bf16 keys, or fp8 keys with fp8 q.
+cudaError_t launch_lean(int heads, int kind, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
+                        const Layout& L, int grid, cudaStream_t s);
 // Scoring followed by the selection of every row in the same kernel (umma_*_topk.cu).
 cudaError_t launch_bf16_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                              const Layout& L, int grid, cudaStream_t s);
@@ -987,17 +1005,17 @@ cudaError_t launch_fp8_topk(int heads, const CUtensorMap& kv, const CUtensorMap&
 cudaError_t launch_q8_topk(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                            const Layout& L, int grid, cudaStream_t s);
 
-template <int H, int KIND, bool FUSE>
+template <int H, int KIND, bool FUSE, bool LEAN>
 cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up, const Layout& L,
                      int grid, cudaStream_t s) {
-  auto kern = umma_score_kernel<H, KIND, FUSE>;
+  auto kern = umma_score_kernel<H, KIND, FUSE, LEAN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.total);
   if (e != cudaSuccess) return e;
   // programmatic stream serialisation: the launch may begin while the
   // previous kernel finishes; the kernel waits for it before touching memory
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(Roles<KIND == kKindFp8Keys>::kThreads, 1, 1);
+  cfg.blockDim = dim3(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)L.total;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -1010,17 +1028,17 @@ cudaError_t launch_h(const CUtensorMap& kv, const CUtensorMap& qm, const UmmaPar
   return cudaGetLastError();
 }
 
-template <int KIND, bool FUSE = false>
+template <int KIND, bool FUSE = false, bool LEAN = false>
 cudaError_t launch_any(int heads, const CUtensorMap& kv, const CUtensorMap& qm, const UmmaParams& up,
                        const Layout& L, int grid, cudaStream_t s) {
   switch (heads) {
-    case 1: return launch_h<1, KIND, FUSE>(kv, qm, up, L, grid, s);
-    case 2: return launch_h<2, KIND, FUSE>(kv, qm, up, L, grid, s);
-    case 4: return launch_h<4, KIND, FUSE>(kv, qm, up, L, grid, s);
-    case 8: return launch_h<8, KIND, FUSE>(kv, qm, up, L, grid, s);
-    case 16: return launch_h<16, KIND, FUSE>(kv, qm, up, L, grid, s);
-    case 32: return launch_h<32, KIND, FUSE>(kv, qm, up, L, grid, s);
-    default: return launch_h<64, KIND, FUSE>(kv, qm, up, L, grid, s);
+    case 1: return launch_h<1, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    case 2: return launch_h<2, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    case 4: return launch_h<4, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    case 8: return launch_h<8, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    case 16: return launch_h<16, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    case 32: return launch_h<32, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
+    default: return launch_h<64, KIND, FUSE, LEAN>(kv, qm, up, L, grid, s);
   }
 }
 

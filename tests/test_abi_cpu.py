@@ -136,12 +136,21 @@ def test_last_error_names_the_problem(lib):
 def test_dispatch_decisions(lib):
     """Host dispatch on host metadata only (vLLM #62589 'Dispatch')."""
     qsa.force_variant(qsa.VARIANT_AUTO)
-    # single-row bf16 decode: the tcgen05 scorer (measured faster at every row count)
-    assert qsa.plan_variant(_desc(rows_per_req=1)) == qsa.VARIANT_UMMA
+    # single-row bf16 decode: the lean tcgen05 form
+    assert qsa.plan_variant(_desc(rows_per_req=1)) == qsa.VARIANT_UMMA_LEAN
     # odd page size: only the CUDA-core scorer serves it
     assert qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256)) == qsa.VARIANT_ROWCORE
-    # MTP verify rows (4 rows x 4 heads = N 16) and fp8 keys -> tcgen05 scorer
-    assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA
+    # MTP verify rows (4 rows x 4 heads = N 16): lean; 256 rows still lean, 260 not
+    assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA_LEAN
+    assert qsa.plan_variant(_desc(num_requests=64)) == qsa.VARIANT_UMMA_LEAN
+    assert qsa.plan_variant(_desc(num_requests=65)) == qsa.VARIANT_UMMA
+    # groups wider than 64 rows x heads (32 rows x 4 heads = N 128), or whose q
+    # leaves the lean form's shared memory fewer than three 32 KB key stages
+    # (bf16 at N 64): the full form
+    assert qsa.plan_variant(_desc(rows_per_req=32)) == qsa.VARIANT_UMMA
+    assert qsa.plan_variant(_desc(rows_per_req=16)) == qsa.VARIANT_UMMA
+    assert qsa.plan_variant(_desc(rows_per_req=8)) == qsa.VARIANT_UMMA_LEAN
+    # fp8 keys (with bf16 q, which qsa_plan_variant assumes): the converter of the full form
     d8 = _desc(rows_per_req=1, num_heads=64, page_cols=64, key_page_stride=64 * 132,
                kv_dtype=qsa.KV_FP8_E4M3, scale_page_stride=64 * 132)
     assert qsa.plan_variant(d8) == qsa.VARIANT_UMMA
@@ -150,9 +159,16 @@ def test_dispatch_decisions(lib):
     qsa.force_variant(qsa.VARIANT_ROWCORE)
     assert qsa.plan_variant(_desc()) == qsa.VARIANT_ROWCORE
     qsa.force_variant(qsa.VARIANT_UMMA)
+    assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA
     with pytest.raises(qsa.QSAError) as e:
         qsa.plan_variant(_desc(page_cols=5, key_page_stride=5 * 256))
     assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
+    qsa.force_variant(qsa.VARIANT_UMMA_LEAN)
+    assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA_LEAN
+    for bad in (d8, _desc(num_requests=65), _desc(rows_per_req=32)):
+        with pytest.raises(qsa.QSAError) as e:
+            qsa.plan_variant(bad)
+        assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "lean" in str(e.value)
     qsa.force_variant(qsa.VARIANT_AUTO)
 
 

@@ -115,7 +115,7 @@ def test_caller_bound_steers_dispatch_only(oracle_mod, max_visible):
     inp = qi.build_inputs(case_spec(case, qi.KV_BF16))
     logits, idx, ran, _ = run_fused(inp, 2048, max_visible=max_visible)
     # unknown (0) and large bounds leave these 30016-column rows to the top-k launch
-    assert ran == (qsa.VARIANT_UMMA_TOPK if max_visible == 1 else qsa.VARIANT_UMMA)
+    assert ran == (qsa.VARIANT_UMMA_TOPK if max_visible == 1 else qsa.VARIANT_UMMA_LEAN)
     check(oracle_mod, inp, logits, idx, 2048, where=f"bound {max_visible}")
     assert workspace_is_zero()
 

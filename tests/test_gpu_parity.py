@@ -19,7 +19,8 @@ pytestmark = pytest.mark.gpu
 import sparse_attention_indexer_02_gb300 as qsa  # noqa: E402
 from sparse_attention_indexer_02_gb300 import torch_api  # noqa: E402
 
-VARIANTS = {"auto": qsa.VARIANT_AUTO, "rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA}
+VARIANTS = {"auto": qsa.VARIANT_AUTO, "rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA,
+            "lean": qsa.VARIANT_UMMA_LEAN}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -42,7 +43,7 @@ def desc_of(inp):
 def supported(inp, variant):
     qsa.force_variant(variant)
     try:
-        qsa.plan_variant(desc_of(inp))
+        qsa.plan_variant(desc_of(inp), inp.spec.q_dtype)
         return True
     except qsa.QSAError as e:
         if e.status == qsa.QSA_ERR_UNSUPPORTED:
@@ -283,7 +284,7 @@ def test_fp8_q_small_shapes_match_oracle(oracle_mod, case, variant):
     assert_topk_strict(idx, oracle_mod.select_topk(g, spec.visible, k), where=name)
 
 
-@pytest.mark.parametrize("variant", ["rowcore", "umma"])
+@pytest.mark.parametrize("variant", ["rowcore", "umma", "lean"])
 def test_fp8_q_exact_integer_case_is_bit_exact(oracle_mod, variant):
     """q and keys in {-3..3}, power-of-two scales and weights: exact in fp32."""
     spec = qi.custom("exact_q8", 2, 4, 4, 16, [300, 301, 302, 303, 17, 18, 19, 0], 320,

@@ -80,3 +80,29 @@ def test_noalloc_matches_the_workspace_call_on_two_calls_in_a_row(case):
         assert torch.equal(got_i, ref_i)
         assert int(ws.abs().sum()) == 0
     assert qsa.device_status(clear=True) == 0
+
+
+class _DeviceWords:
+    """int32 view of device memory the library owns (zero-copy, through the
+    CUDA array interface), so the test can write the counter array directly."""
+
+    def __init__(self, ptr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False), "version": 2,
+                                         "strides": None}
+
+
+def test_device_status_clear_zeroes_counters_a_failed_call_left():
+    """A no-alloc call that gave up on a barrier (qsa_device_status bit 0) may
+    leave counts in the array; here they are planted from the host instead.
+    qsa_device_status(clear) zeroes the array, and the next calls match the
+    workspace call again."""
+    addr, nbytes = _abi.noalloc_counters()
+    assert addr != 0 and nbytes == 4 * 257
+    words = torch.as_tensor(_DeviceWords(addr, nbytes // 4), device="cuda")
+    words.copy_(torch.arange(1, nbytes // 4 + 1, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert int(words.abs().sum()) > 0
+    assert qsa.device_status(clear=True) == 0
+    assert int(words.abs().sum()) == 0
+    test_noalloc_matches_the_workspace_call_on_two_calls_in_a_row(CASES[0])
+    assert int(words.abs().sum()) == 0
