@@ -262,14 +262,15 @@ def oracle_sample_run(inp, requests, threads):
     return dt, key_bytes, len(rows)
 
 
-def cpu_baseline(inp, budget_s: float = 10.0):
-    """The oracle on the host cores: whole requests (scoring + top-k), repeated
-    until about budget_s seconds of work; prefill-sized requests are sampled by
-    rows instead.  Returns key-cache GB/s over the sample."""
+def cpu_baseline(inp, budget_s: float = 10.0, threads=None):
+    """The oracle on the host cores (all of them, or `threads`): whole requests
+    (scoring + top-k), repeated until about budget_s seconds of work;
+    prefill-sized requests are sampled by rows instead.  Returns key-cache GB/s
+    over the sample."""
     import oracle
 
     oracle.build()
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     spec = inp.spec
     rng = np.random.default_rng(0)
     order = rng.permutation(spec.num_requests).tolist()
@@ -362,13 +363,170 @@ def workload_config(spec: qi.Spec, l2_note):
 # ---------------------------------------------------------------------------
 
 
+def stats(samples):
+    """median / min / max of per-launch times (µs), and how many launches."""
+    v = sorted(x for x, _ in samples)
+    return {"median": round(statistics.median(v), 3), "min": round(v[0], 3), "max": round(v[-1], 3),
+            "launches": int(sum(n for _, n in samples))}
+
+
+def build_record():
+    """Units build.py had to compile without ptxas optimisation (its fallback
+    when the compiler crashes); empty for a normal build."""
+    from sparse_attention_indexer_02_gb300 import build as qbuild
+
+    return {"ptxas_O0_units": qbuild.o0_units()}
+
+
+SWEEP = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "mtp3_large_p16",
+         "mtp3_large_p64", "fp8_h64", "prefill_chunk", "fp8q_h64", "ragged_nn8"]
+
+
+class Workload:
+    """One workload on the device: rotating input/output copies (their
+    footprint over twice the L2), the three call forms, and graphs of them."""
+
+    def __init__(self, name, dev, rank=0, rotate=True):
+        import torch
+        from sparse_attention_indexer_02_gb300 import torch_api
+
+        base = qi.WORKLOADS[name]()
+        self.spec = spec = dataclasses.replace(base, seed=base.seed + 7919 * rank)  # per-rank data, same shape
+        self.inp = inp = qi.build_inputs(spec)
+        self.host = qi.device_tensors(inp, pin=True)
+        self.dev = dev
+        R, k = spec.num_rows, spec.k
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        per_copy = inp.kv.nbytes + R * spec.out_cols * 4 + inp.q.nbytes + R * k * 4
+        self.copies = copies = 1 if not rotate else int(min(16, max(1, math.ceil(2.0 * l2 / per_copy))))
+        self.sets = []
+        for _ in range(copies):
+            d = {n: t.to(dev, non_blocking=False) for n, t in self.host.items()}
+            d["out"] = torch.empty((R, spec.out_cols), dtype=torch.float32, device=dev)
+            d["idx"] = torch.empty((R, k), dtype=torch.int32, device=dev)
+            self.sets.append(d)
+        self.l2_note = (f"rotating {copies} input/output copies ({copies * per_copy / 1e6:.0f} MB, > 2x the "
+                        f"{l2 / 1e6:.0f} MB L2)" if copies > 1 else
+                        f"single copy ({per_copy / 1e6:.0f} MB of inputs+outputs, larger than 2x L2)"
+                        if per_copy > 2 * l2 else f"single copy ({per_copy / 1e6:.0f} MB), L2 not defeated")
+        self.max_visible = int(spec.live_visible().max()) if R else 0
+        self.api = torch_api
+        self.per_graph = copies * max(1, -(-16 // copies))
+
+    def score(self, d):
+        s = self.spec
+        self.api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
+                                  page_cols=s.page_cols, out_cols=s.out_cols, kv_dtype=s.kv_dtype,
+                                  scale_offset=self.inp.scale_offset, out=d["out"], next_n_lens=d.get("next_n_lens"))
+
+    def topk(self, d):  # ragged call: the top-k reads the live rows' visible counts
+        self.api.select_topk(d["out"], d.get("visible_live", d["visible"]), self.spec.k, out=d["idx"])
+
+    def one_call(self, d):
+        # qsa_paged_mqa_topk; the host bound of the visible counts steers its
+        # dispatch (the selection inside the scoring kernel for decode-sized calls)
+        s = self.spec
+        self.api.paged_mqa_topk(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"], s.k,
+                                page_cols=s.page_cols, out_cols=s.out_cols, kv_dtype=s.kv_dtype,
+                                scale_offset=self.inp.scale_offset, max_visible=self.max_visible,
+                                out_logits=d["out"], out_idx=d["idx"], next_n_lens=d.get("next_n_lens"))
+
+    def step(self, d, form):
+        if form == "one-call":
+            self.one_call(d)
+        else:
+            self.score(d)
+            self.topk(d)
+
+    def capture(self, n, what):
+        import torch
+
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                d = self.sets[i % self.copies]
+                if what == "score":
+                    self.score(d)
+                elif what == "topk":
+                    self.topk(d)
+                else:
+                    self.step(d, what)
+        return g
+
+    def time_graph(self, g, n_launch, reps):
+        """Per-launch mean of each of `reps` replays of a graph of n_launch calls."""
+        import torch
+
+        stream = torch.cuda.current_stream(self.dev)
+        for _ in range(2):
+            g.replay()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        torch.cuda.synchronize(self.dev)
+        ev[0].record(stream)
+        for i in range(reps):
+            g.replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize(self.dev)
+        return [(1e3 * ev[i].elapsed_time(ev[i + 1]) / n_launch, n_launch) for i in range(reps)]
+
+    def kernel_stats(self, min_launches=64):
+        """scoring, top-k, two-call step and one-call step: per-launch median/min/max."""
+        import sparse_attention_indexer_02_gb300 as qsa
+        import torch
+
+        for i in range(3):  # eager first calls (kernel attributes; the one-call workspace)
+            d = self.sets[i % self.copies]
+            self.score(d)
+            self.topk(d)
+        variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
+        for i in range(3):
+            self.one_call(self.sets[i % self.copies])
+        one_variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
+        torch.cuda.synchronize(self.dev)
+        n = self.per_graph
+        reps = max(4, -(-min_launches // n))
+        out = {"variant": variant, "one_call_variant": one_variant}
+        for key, what in (("scoring_us", "score"), ("topk_us", "topk"), ("step_us", "two-call"),
+                          ("one_call_us", "one-call")):
+            g = self.capture(n, what)
+            out[key] = stats(self.time_graph(g, n, reps))
+            del g
+        return out
+
+    def summary(self, ks, peaks):
+        """The per-workload entry of the bench line."""
+        spec = self.spec
+        sb, tb = algorithmic_bytes(spec)
+        key_bytes = spec.key_bytes_touched()
+        t_score = ks["scoring_us"]["median"] * 1e-6
+        t_topk = ks["topk_us"]["median"] * 1e-6
+        e = {"config": workload_config(spec, self.l2_note), **ks,
+             "key_gbs_scoring": round(key_bytes / t_score / 1e9, 1),
+             "frac_key_bytes": round(key_bytes / t_score / 1e9 / peaks["hbm_gbs"], 4),
+             "frac_all_bytes": round(sum(sb.values()) / t_score / 1e9 / peaks["hbm_gbs"], 4),
+             "topk_gbs": round(sum(tb.values()) / t_topk / 1e9, 1),
+             "topk_frac": round(sum(tb.values()) / t_topk / 1e9 / peaks["hbm_gbs"], 4),
+             "topk_us_per_row": round(ks["topk_us"]["median"] / spec.num_rows, 4)}
+        flops = 2 * spec.head_dim * spec.num_heads * int(spec.live_visible().astype(np.int64).sum())
+        if spec.rows_per_req > 64:  # the contraction-heavy case: tensor-core rate too
+            e["mma_tflops"] = round(flops / t_score / 1e12, 1)
+            e["frac_bf16_peak"] = round(flops / t_score / 1e12 / peaks["bf16_tflops"], 4)
+        return e
+
+    def free(self):
+        import torch
+
+        self.sets = []
+        self.host = None
+        torch.cuda.empty_cache()
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     import sparse_attention_indexer_02_gb300 as qsa
     from sparse_attention_indexer_02_gb300 import build as qbuild
-    from sparse_attention_indexer_02_gb300 import torch_api
 
     rank, world, local = rank_env()
     if world > 1:
@@ -380,79 +538,26 @@ def run_gpu(args):
     if args.variant != "auto":
         qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA,
                            "lean": qsa.VARIANT_UMMA_LEAN}[args.variant])
+    peaks = measured_peaks()
 
-    base = qi.WORKLOADS[args.workload]()
-    spec = dataclasses.replace(base, seed=base.seed + 7919 * rank)  # per-rank data, same shape
-    inp = qi.build_inputs(spec)
-    host = qi.device_tensors(inp, pin=True)
+    W = Workload(args.workload, dev, rank, rotate=not args.no_rotate)
+    spec, inp, host, sets, copies = W.spec, W.inp, W.host, W.sets, W.copies
     R, k = spec.num_rows, spec.k
-
-    # rotation: enough copies that one step's data is out of L2 by its next use
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_copy = inp.kv.nbytes + R * spec.out_cols * 4 + inp.q.nbytes + R * k * 4
-    copies = 1 if args.no_rotate else int(min(16, max(1, math.ceil(2.0 * l2 / per_copy))))
-    sets = []
-    for _ in range(copies):
-        d = {name: t.to(dev, non_blocking=False) for name, t in host.items()}
-        d["out"] = torch.empty((R, spec.out_cols), dtype=torch.float32, device=dev)
-        d["idx"] = torch.empty((R, k), dtype=torch.int32, device=dev)
-        sets.append(d)
-    l2_note = (f"rotating {copies} input/output copies ({copies * per_copy / 1e6:.0f} MB, > 2x the "
-               f"{l2 / 1e6:.0f} MB L2)" if copies > 1 else
-               f"single copy ({per_copy / 1e6:.0f} MB of inputs+outputs, larger than 2x L2)"
-               if per_copy > 2 * l2 else f"single copy ({per_copy / 1e6:.0f} MB), L2 not defeated")
-
-    def score(d):
-        torch_api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
-                                   page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
-                                   scale_offset=inp.scale_offset, out=d["out"], next_n_lens=d.get("next_n_lens"))
-
-    def topk(d):  # ragged call: the top-k reads the live rows' visible counts
-        torch_api.select_topk(d["out"], d.get("visible_live", d["visible"]), k, out=d["idx"])
-
-    # the same step as one qsa_paged_mqa_topk call; the host bound of the
-    # visible counts steers its dispatch (the selection inside the scoring
-    # kernel for decode-sized calls)
-    max_visible = int(spec.live_visible().max()) if R else 0
-
-    def fused(d):
-        torch_api.paged_mqa_topk(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"], k,
-                                 page_cols=spec.page_cols, out_cols=spec.out_cols, kv_dtype=spec.kv_dtype,
-                                 scale_offset=inp.scale_offset, max_visible=max_visible, out_logits=d["out"],
-                                 out_idx=d["idx"], next_n_lens=d.get("next_n_lens"))
-
-    # eager warm-up (first calls set kernel attributes), then CUDA graphs: the
-    # host enqueues one graph per >= 16 steps, so launch overhead on the host
-    # never shows up in the device timings.
-    fused_step = args.step == "fused"
-    for i in range(args.warmup):
+    form = "one-call" if args.step == "fused" else "two-call"
+    for i in range(args.warmup):  # eager warm-up (first calls set kernel attributes)
         d = sets[i % copies]
-        score(d)
-        topk(d)
-        if fused_step:
-            fused(d)
-    variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
+        W.score(d)
+        W.topk(d)
+        W.one_call(d)
     torch.cuda.synchronize(dev)
 
-    def capture(n_steps, do_score=True, do_topk=True):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for i in range(n_steps):
-                d = sets[i % copies]
-                if do_score and do_topk and fused_step:
-                    fused(d)
-                    continue
-                if do_score:
-                    score(d)
-                if do_topk:
-                    topk(d)
-        return g
-
+    # the timed region: K steps as graph replays (>= 16 steps a graph), so host
+    # launch overhead is not on the device timeline
     K = args.steps
-    per_graph = copies * max(1, -(-16 // copies))
+    per_graph = W.per_graph
     full_graphs, rem = divmod(K, per_graph)
-    g_step = capture(per_graph)
-    g_rem = capture(rem) if rem else None
+    g_step = W.capture(per_graph, form)
+    g_rem = W.capture(rem, form) if rem else None
     for _ in range(max(1, -(-args.warmup // per_graph))):
         g_step.replay()
     torch.cuda.synchronize(dev)
@@ -475,48 +580,23 @@ def run_gpu(args):
     barrier()
     clocks = sampler.stop(t0, t1) if sampler else None
     total_ms = e_start.elapsed_time(e_end)
+    del g_step, g_rem
 
-    # per-kernel launch times: graphs of scoring launches only / top-k only
-    def time_graph(g, n_launch, reps):
-        for _ in range(2):
-            g.replay()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for _ in range(reps):
-            g.replay()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        return 1e3 * a.elapsed_time(b) / (reps * n_launch)
-
-    reps = max(1, min(full_graphs, 64))
-    g_score = capture(per_graph, do_topk=False)
-    g_topk = capture(per_graph, do_score=False)
-    score_us = time_graph(g_score, per_graph, reps)
-    topk_us = time_graph(g_topk, per_graph, reps)
-    del g_step, g_rem, g_score, g_topk
-    # the one-call form (eager first: its workspace is allocated outside capture)
-    for i in range(3):
-        fused(sets[i % copies])
-    fused_variant = qsa.VARIANT_NAMES.get(qsa.last_variant(), "none")
-    torch.cuda.synchronize(dev)
-    g_fused = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_fused):
-        for i in range(per_graph):
-            fused(sets[i % copies])
-    fused_us = time_graph(g_fused, per_graph, reps)
-    del g_fused
+    # per-kernel launch times on the same workload (median/min/max over replays)
+    ks = W.kernel_stats()
+    head = W.summary(ks, peaks)
 
     max_ms = max_over_ranks(total_ms)
     ms_step = max_ms / K
     key_bytes = spec.key_bytes_touched()
     value = sum_over_ranks(key_bytes * K) / (max_ms / 1e3) / 1e9
 
-    # roofline of the dominant kernel
-    peaks = measured_peaks()
+    # roofline of the dominant kernel of the step
     sb, tb = algorithmic_bytes(spec)
-    if fused_step:  # one kernel: its bytes are the scoring's and the selection's
-        kname, kbytes, kus = variant, sum(sb.values()) + sum(tb.values()), fused_us
+    variant = ks["variant"]
+    score_us, topk_us = ks["scoring_us"]["median"], ks["topk_us"]["median"]
+    if form == "one-call":  # one kernel: its bytes are the scoring's and the selection's
+        kname, kbytes, kus = ks["one_call_variant"], sum(sb.values()) + sum(tb.values()), ks["one_call_us"]["median"]
     elif score_us >= topk_us:
         kname, kbytes, kus = variant, sum(sb.values()), score_us
     else:
@@ -525,15 +605,15 @@ def run_gpu(args):
     traffic = recorded_traffic(kname, spec.name) if kname in KERNEL_SOURCES else None
     roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                "algorithmic_bytes": int(kbytes), "peak_source": f"{peaks['source']} (copy bandwidth)"}
+                "algorithmic_bytes": int(kbytes), "peak_source": f"{peaks['source']} (copy bandwidth)",
+                "key_bytes_frac": head["frac_key_bytes"] if kname != "topk" else None}
 
     # end to end through the public API with host buffers: H2D of every input
     # from pinned memory, both calls, D2H of the top-k indices, every step
     e2e = None
     if not args.no_e2e:
-        # every step copies all of its inputs host -> device (pinned memory) and
-        # reads its selection back; two input buffers let step i+1's copies run
-        # on a copy stream while step i's kernels run
+        # two input buffers let step i+1's copies run on a copy stream while
+        # step i's kernels run
         bufs = [sets[0], sets[1 % copies] if copies > 1 else
                 {name: torch.empty_like(t) for name, t in sets[0].items()}]
         out_host = [torch.empty((R, k), dtype=torch.int32).pin_memory() for _ in range(2)]
@@ -555,11 +635,7 @@ def run_gpu(args):
                     b[name].copy_(t, non_blocking=True)
                 ready[i % 2].record(cstream)
             comp.wait_event(ready[i % 2])
-            if fused_step:
-                fused(b)
-            else:
-                score(b)
-                topk(b)
+            W.step(b, form)
             out_host[i % 2].copy_(b["idx"], non_blocking=True)
             free[i % 2].record(comp)
 
@@ -584,6 +660,23 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp)
+        one = cpu_baseline(inp, budget_s=5.0, threads=1)
+        cpu["single_thread"] = {"value": one["value"], "unit": one["unit"], "cores": 1, "sample": one["sample"],
+                                "seconds": one["seconds"]}
+    W.free()
+    del W, sets, host
+
+    # every configuration of the workload statement (and the ragged and fp8-q
+    # calls), timed the same way, one after another
+    workloads = {spec.name: head}
+    if rank == 0 and not args.no_workloads:
+        for name in SWEEP:
+            if name == args.workload:
+                continue
+            Wn = Workload(name, dev, rank, rotate=not args.no_rotate)
+            workloads[Wn.spec.name] = Wn.summary(Wn.kernel_stats(), peaks)
+            Wn.free()
+            del Wn
 
     if rank == 0:
         line = {
@@ -592,14 +685,15 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": ("bf16" if spec.kv_dtype == qi.KV_BF16 else
                                            "fp8e4m3-keys/bf16-q" if spec.q_dtype == qi.Q_BF16 else "fp8e4m3"),
             "data": "synthetic (seeded; shapes of the pages' workloads)",
-            "config": workload_config(spec, l2_note),
+            "config": head["config"],
             "variant": variant,
-            "us_per_call": round(score_us, 3), "key_gbs_scoring": round(key_bytes / (score_us * 1e-6) / 1e9, 1),
-            "topk_us_per_row": round(topk_us / R, 4), "topk_us_per_call": round(topk_us, 3),
+            "us_per_call": score_us, "key_gbs_scoring": head["key_gbs_scoring"],
+            "topk_us_per_row": head["topk_us_per_row"], "topk_us_per_call": topk_us,
             "step_us": round(1e3 * ms_step, 3),
-            "fused_step_us": round(fused_us, 3), "fused_variant": fused_variant,
+            "fused_step_us": ks["one_call_us"]["median"], "fused_variant": ks["one_call_variant"],
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if fused_step else 2) * K, "clocks": clocks,
+            "gpu_launches": (1 if form == "one-call" else 2) * K, "clocks": clocks,
+            "build": build_record(), "workloads": workloads,
         }
         print(json.dumps(line))
     if world > 1:
@@ -621,6 +715,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the per-workload timings of the other configurations")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -222,9 +222,10 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
  *                (unknown; out_cols and the page capacity bound them).  Like
  *                vLLM #62589's single_row_decode flag it only steers the
  *                dispatch: the selection runs in the scoring kernel for at
- *                most 256 rows whose bound is at most 16384 columns, and as a
- *                separate top-k launch (which splits long rows over a thread-
- *                block cluster) otherwise.  A wrong bound costs speed only.
+ *                most 256 rows, one row a request, whose bound is at most
+ *                16384 columns, and as a separate top-k launch (which splits
+ *                long rows over a thread-block cluster) otherwise.  A wrong
+ *                bound costs speed only.
  *   out_idx      int32 [R][k] (device), 4-byte aligned.
  *   workspace    device memory of at least qsa_paged_mqa_topk_workspace(desc)
  *                bytes, 4-byte aligned (NULL when that size is 0).  It must
@@ -242,7 +243,8 @@ qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* desc, int32_t q_dtype, const
                               size_t workspace_bytes, void* stream);
 
 /* Workspace bytes qsa_paged_mqa_topk needs for `desc` (host only; 0 when the
- * shape never runs the fused selection): 4 * (2 * G + 1) for the G <= 256 row
+ * shape never runs the fused selection, e.g. several rows a request, unless
+ * QSA_VARIANT_UMMA_TOPK is forced): 4 * (2 * G + 1) for the G <= 256 row
  * groups of the tcgen05 scorer. */
 qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* bytes);
 
@@ -305,8 +307,12 @@ qsa_status qsa_plan_variant(const qsa_paged_desc* desc, int32_t* variant);
 qsa_status qsa_plan_variant_ex(const qsa_paged_desc* desc, int32_t q_dtype, int32_t* variant);
 
 /* Force a variant for later calls (QSA_VARIANT_AUTO restores the dispatch).
- * A forced variant that cannot serve a shape makes the call return
- * QSA_ERR_UNSUPPORTED.  Meant for tests and A/B measurements. */
+ * A forced scorer (ROWCORE, UMMA, UMMA_LEAN) that cannot serve a shape makes
+ * the call return QSA_ERR_UNSUPPORTED, and qsa_paged_mqa_topk then runs it
+ * and the top-k launch.  QSA_VARIANT_UMMA_TOPK makes qsa_paged_mqa_topk select
+ * inside the scoring kernel for every shape the tcgen05 scorer serves (the
+ * dispatch does so for single-row groups only) and leaves the scoring calls'
+ * dispatch as it is.  Meant for tests and A/B measurements. */
 void qsa_force_variant(int32_t variant);
 
 /* Variant launched by this thread's last successful scoring call

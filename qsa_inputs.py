@@ -328,13 +328,27 @@ def random_logit_rows(rng: np.random.Generator, num_rows: int, width: int,
     return x
 
 
-def gather_rows_for(spec: Spec, max_rows: int, rng: np.random.Generator) -> List[int]:
-    """A stratified sample of row indices (first, last and random rows)."""
+def gather_rows_for(spec: Spec, max_rows: int, rng: np.random.Generator, group_rows: int = 0,
+                    edge_groups: int = 0) -> List[int]:
+    """A stratified sample of row indices: the first and last rows; with
+    group_rows, the edge rows (first and last, and the row before) of the first
+    three and of `edge_groups` more groups of `group_rows` consecutive rows
+    spread over the batch, the last group among them; then random rows, up to
+    max_rows or at least four of them past the edge rows."""
     R = spec.num_rows
     if R <= max_rows:
         return list(range(R))
     picks = {0, R - 1}
-    while len(picks) < max_rows:
+    if group_rows > 0 and edge_groups > 0:
+        n_groups = -(-R // group_rows)
+        spread = np.linspace(0, n_groups - 1, edge_groups).round().astype(int).tolist()
+        for g in sorted(set([0, 1, 2] + spread) & set(range(n_groups))):
+            first = int(g) * group_rows
+            picks.update({first, min(R, first + group_rows) - 1})
+            if first > 0:
+                picks.add(first - 1)
+    target = min(R, max(max_rows, len(picks) + 4))
+    while len(picks) < target:
         picks.add(int(rng.integers(0, R)))
     return sorted(picks)
 

@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import json
 import os
 import resource
 import shutil
@@ -57,11 +58,15 @@ def _raise_stack_limit():
         pass
 
 
-def _compile(src: str) -> str:
+O0_RECORD = os.path.join(BUILD, "ptxas_O0_units.json")
+
+
+def _compile(src: str):
     unit = os.path.splitext(os.path.basename(src))[0]
     obj = os.path.join(BUILD, unit + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True, preexec_fn=_raise_stack_limit)
+    o0 = False
     if res.returncode in (139, -11) or "Segmentation fault" in res.stderr:
         # the compiler itself crashed (seen with ptxas 13.0 on aarch64 hosts):
         # rebuild this unit without ptxas optimisation rather than fail the build
@@ -69,11 +74,22 @@ def _compile(src: str) -> str:
                          f"-Xptxas -O0 (correct but slower code)\n")
         res = subprocess.run(cmd[:-3] + ["-Xptxas", "-O0"] + cmd[-3:], capture_output=True, text=True,
                              preexec_fn=_raise_stack_limit)
+        o0 = True
     with open(os.path.join(BUILD, f"ptxas_{unit}.log"), "w") as f:
         f.write(res.stdout + res.stderr)
     if res.returncode != 0:
         raise RuntimeError(f"nvcc failed on {unit}.cu:\n{res.stderr[-4000:]}")
-    return obj
+    return obj, (unit if o0 else None)
+
+
+def o0_units() -> list:
+    """Units of the current libqsa.so that build() compiled with -Xptxas -O0
+    because the optimising compiler crashed (normally none)."""
+    try:
+        with open(O0_RECORD) as f:
+            return list(json.load(f))
+    except (OSError, ValueError):
+        return []
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -82,7 +98,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(_compile, srcs))
+        done = list(ex.map(_compile, srcs))
+    objs = [o for o, _ in done]
+    with open(O0_RECORD, "w") as f:
+        json.dump(sorted(u for _, u in done if u), f)
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)

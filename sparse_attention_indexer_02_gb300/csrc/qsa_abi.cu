@@ -253,10 +253,23 @@ qsa_status launch_scoring(const qsa::ScoreParams& p, int32_t variant, cudaStream
 constexpr int64_t kFuseMaxRows = 256;
 constexpr int64_t kFuseMaxVisible = 16384;
 
+// Whether qsa_paged_mqa_topk may select inside the scoring kernel for `d`
+// (the row count and the caller's bound are checked at the call).  Measured on
+// GB300, the fused kernel is slower than the lean scorer and the top-k launch
+// for groups of several rows (tiny_mtp 12.1 vs 9.4 us), so the dispatch fuses
+// single-row groups only; QSA_VARIANT_UMMA_TOPK forced fuses every shape the
+// tcgen05 scorer serves, and any other forced variant none.
+bool fusable(const qsa_paged_desc* d) {
+  const char* why = nullptr;
+  if (!qsa::umma_supports(*d, &why)) return false;
+  const int32_t forced = g_forced_variant.load();
+  if (forced == QSA_VARIANT_UMMA_TOPK) return true;
+  return forced == QSA_VARIANT_AUTO && d->rows_per_req == 1;
+}
+
 // Workspace words of the fused selection for `d` (0: the shape is never fused).
 int64_t fused_words(const qsa_paged_desc* d) {
-  const char* why = nullptr;
-  if (!qsa::umma_supports(*d, &why)) return 0;
+  if (!fusable(d)) return 0;
   const int64_t G = qsa::umma_num_groups(*d);
   return G >= 1 && G <= qsa::kFuseMaxGroups ? 2 * G + 1 : 0;
 }
@@ -317,11 +330,9 @@ qsa_status topk_call(const qsa_paged_desc* d, int32_t q_dtype, const void* q, co
   if (!noalloc && words > 0 && (!workspace || !aligned(workspace, 4) || workspace_bytes < (size_t)words * 4))
     return fail(QSA_ERR_INVALID_ARG, "workspace must be 4-byte aligned and hold %lld bytes", (long long)words * 4);
   const int64_t bound = max_visible > 0 && max_visible < p.capacity ? max_visible : p.capacity;
-  // the fused selection runs in the full form of the tcgen05 scorer (the lean
-  // form is taken for the scoring alone unless it was forced)
-  const bool tc = variant == QSA_VARIANT_UMMA ||
-                  (variant == QSA_VARIANT_UMMA_LEAN && g_forced_variant.load() == QSA_VARIANT_AUTO);
-  const bool fused = tc && words > 0 && p.num_rows <= kFuseMaxRows && bound <= kFuseMaxVisible;
+  // the fused selection runs in the full form of the tcgen05 scorer
+  const bool fused =
+      words > 0 && variant != QSA_VARIANT_ROWCORE && p.num_rows <= kFuseMaxRows && bound <= kFuseMaxVisible;
   if (fused && noalloc) {
     if (words > kNoAllocWords)
       return fail(QSA_ERR_UNSUPPORTED,

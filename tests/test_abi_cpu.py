@@ -174,7 +174,7 @@ def test_dispatch_decisions(lib):
 
 def test_fused_call_workspace_size_and_argument_checks(lib):
     """qsa_paged_mqa_topk: host checks before anything is enqueued."""
-    d = _desc()  # 2 requests x 4 rows x 4 heads: one row group a request
+    d = _desc(rows_per_req=1)  # 2 single-row requests: two row groups
     assert qsa.topk_workspace_bytes(d) == 4 * (2 * 2 + 1)
     # the CUDA-core scorer's shapes never run the fused selection
     assert qsa.topk_workspace_bytes(_desc(page_cols=5, key_page_stride=5 * 256)) == 0
@@ -197,6 +197,26 @@ def test_fused_call_workspace_size_and_argument_checks(lib):
     assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
     qsa.paged_mqa_topk(_desc(num_requests=0), None, None, None, None, None, None, 8, None, None, None, 0,
                        stream=0)  # no rows: nothing to do
+
+
+def test_one_call_fuses_single_row_groups_only(lib):
+    """The dispatch of qsa_paged_mqa_topk: the selection inside the scoring
+    kernel for single-row requests (a workspace is needed), the two launches
+    for several rows a request (measured faster; no workspace) unless
+    QSA_VARIANT_UMMA_TOPK is forced, and never for a forced scorer."""
+    qsa.force_variant(qsa.VARIANT_AUTO)
+    try:
+        assert qsa.topk_workspace_bytes(_desc(rows_per_req=1)) == 4 * (2 * 2 + 1)
+        assert qsa.topk_workspace_bytes(_desc()) == 0
+        assert qsa.topk_workspace_bytes(_desc(rows_per_req=1, page_cols=5, key_page_stride=5 * 256)) == 0
+        qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
+        assert qsa.topk_workspace_bytes(_desc()) == 4 * (2 * 2 + 1)
+        assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA_LEAN  # scoring dispatch unchanged
+        for forced in (qsa.VARIANT_UMMA, qsa.VARIANT_UMMA_LEAN, qsa.VARIANT_ROWCORE):
+            qsa.force_variant(forced)
+            assert qsa.topk_workspace_bytes(_desc(rows_per_req=1)) == 0
+    finally:
+        qsa.force_variant(qsa.VARIANT_AUTO)
 
 
 def test_noalloc_call_rejects_shapes_past_its_counters(lib):

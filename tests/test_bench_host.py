@@ -21,3 +21,18 @@ def test_source_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.source_sha(["k.cu"]) == a
     (tmp_path / "k.cu").write_text("__global__ void k(int* p) { p[0] = 2; }\n")
     assert bench.source_sha(["k.cu"]) != a
+
+
+def test_stats_median_min_max_and_launch_count():
+    s = bench.stats([(3.0, 16), (1.0, 16), (2.0, 16), (10.0, 16)])
+    assert s == {"median": 2.5, "min": 1.0, "max": 10.0, "launches": 64}
+
+
+def test_o0_record_reads_back(tmp_path, monkeypatch):
+    from sparse_attention_indexer_02_gb300 import build as qbuild
+
+    rec = tmp_path / "rec.json"
+    monkeypatch.setattr(qbuild, "O0_RECORD", str(rec))
+    assert qbuild.o0_units() == []
+    rec.write_text('["umma_bf16"]')
+    assert qbuild.o0_units() == ["umma_bf16"]

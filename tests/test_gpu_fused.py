@@ -31,6 +31,16 @@ def _cuda():
     qsa.force_variant(qsa.VARIANT_AUTO)
 
 
+@pytest.fixture(autouse=True)
+def _fuse_every_shape():
+    """The dispatch fuses single-row requests only; these tests cover the fused
+    kernel on every shape it serves, so they force it (tests of the dispatch
+    itself set AUTO)."""
+    qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
+    yield
+    qsa.force_variant(qsa.VARIANT_AUTO)
+
+
 def scored_visible(spec):
     """n[r]: the row's visible count as scored (live rows, clamped to the row)."""
     cap = min(spec.out_cols, spec.max_pages * spec.page_cols)
@@ -223,7 +233,7 @@ def test_fused_call_with_the_cuda_core_scorer(oracle_mod):
     try:
         logits, idx, ran, _ = run_fused(inp, inp.spec.k, max_visible=int(inp.spec.visible.max()))
     finally:
-        qsa.force_variant(qsa.VARIANT_AUTO)
+        qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
     assert ran == qsa.VARIANT_ROWCORE
     check(oracle_mod, inp, logits, idx, inp.spec.k, where="rowcore composition")
     assert workspace_is_zero()
@@ -240,6 +250,22 @@ def test_fused_full_size_decode_workloads(oracle_mod, name):
     assert ran == qsa.VARIANT_UMMA_TOPK
     check(oracle_mod, inp, logits, idx, spec.k, where=f"{name} full size")
     assert workspace_is_zero()
+
+
+@pytest.mark.parametrize("case,fused", [(CASES[0], True), (CASES[2], False), (CASES[3], False)],
+                         ids=["single_row", "mtp4", "rows16"])
+def test_auto_dispatch_fuses_single_row_requests_only(oracle_mod, case, fused):
+    """AUTO: single-row requests select inside the scoring kernel; several rows
+    a request take the lean scorer and the top-k launch (measured faster)."""
+    qsa.force_variant(qsa.VARIANT_AUTO)
+    inp = qi.build_inputs(case_spec(case, qi.KV_BF16))
+    k = case[7]
+    logits, idx, ran, _ = run_fused(inp, k, max_visible=int(inp.spec.visible.max()))
+    s = inp.spec
+    scorer = qsa.plan_variant(qsa.make_desc(s.num_requests, s.rows_per_req, s.num_heads, s.page_cols, s.max_pages,
+                                            inp.num_pages, s.out_cols, inp.key_page_stride))
+    assert ran == (qsa.VARIANT_UMMA_TOPK if fused else scorer)
+    check(oracle_mod, inp, logits, idx, k, where=f"auto {case[0]}")
 
 
 def test_no_fused_kernel_gave_up_on_a_barrier():

@@ -545,7 +545,13 @@ def test_topk_visible_beyond_stride_is_clamped():
 # --------------------------------------------------------------------------
 
 FULL = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "fp8_h64", "prefill_chunk",
-        "mtp3_large_p64", "ragged_nn8", "fp8q_h64"]
+        "mtp3_large_p16", "mtp3_large_p64", "ragged_nn8", "fp8q_h64"]
+
+
+def scorer_group_rows(spec):
+    """Rows the tcgen05 scorer stacks into one MMA (rows x heads <= 256, within
+    a request): the sample takes both edge rows of several such groups."""
+    return min(max(1, 256 // spec.num_heads), spec.rows_per_req)
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -553,7 +559,11 @@ def test_full_size_workload_sampled(oracle_mod, name):
     spec = qi.WORKLOADS[name]()
     inp = qi.build_inputs(spec)
     out, ran, d = gpu_logits(inp)
-    rows = qi.gather_rows_for(spec, 6 if spec.num_heads > 4 else 12, np.random.default_rng(1))
+    # first, last and random rows, and the edge rows of 8 row groups spread
+    # over the batch (the last group included): 63/64, 127/128, ... for the
+    # prefill chunk's 64-row groups, a request's first and last rows for MTP
+    rows = qi.gather_rows_for(spec, 6 if spec.num_heads > 4 else 12, np.random.default_rng(1),
+                              group_rows=scorer_group_rows(spec), edge_groups=8)
     ref = oracle_mod.paged_mqa_logits(inp, rows=rows)
     sub = out[torch.tensor(rows, device="cuda")].cpu().numpy()
     assert_logits_match(sub, ref, spec.kv_dtype, where=f"{name} rows {rows}")

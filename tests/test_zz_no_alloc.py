@@ -20,6 +20,10 @@ def _cuda():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     qsa.load_library()
+    # the counters serve the selection inside the scoring kernel, which the
+    # dispatch runs for single-row requests only: force it for every case
+    qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
+    yield
     qsa.force_variant(qsa.VARIANT_AUTO)
 
 
