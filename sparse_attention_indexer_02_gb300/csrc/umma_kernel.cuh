@@ -62,6 +62,10 @@ constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
 constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
 constexpr int kFp8StageAlloc = kFp8StageBytes + 1024;  // + the block's 128 fp32 scales, 1024-aligned
 constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (see the converter)
+// fp8 q: the copies put each tile's key scales in their own slot of a ring (a
+// slot per tile, reused kQ8Ring tiles later), so a key stage is free as soon
+// as the MMA has read it; at most kQ8Ring - 2 key stages (see the producer).
+constexpr int kQ8Ring = 10;
 // Warp roles: 0 TMA, 1 MMA, then the epilogue warps (three per TMEM lane
 // quadrant, or one with the fp8 -> bf16 converter or in the lean form), then
 // 8 converter warps (fp8 keys with bf16 q) or 2 spare warps that write the
@@ -129,23 +133,26 @@ struct Layout {
 };
 
 inline Layout make_layout(int N, int groups, int kind, bool fused = false, bool lean = false) {
-  const bool fp8 = kind != kKindBf16, conv = kind == kKindFp8Keys;
+  const bool conv = kind == kKindFp8Keys, q8 = kind == kKindFp8Q;
   Layout L;
   L.n = N;
   L.tmem_cols = 2 * N < 32 ? 32 : 2 * N;
-  L.idesc = kind == kKindFp8Q ? ptx::idesc_e4m3_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N);
-  L.stage_bytes = fp8 ? kFp8StageAlloc : kTileBytes;
+  L.idesc = q8 ? ptx::idesc_e4m3_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N);
+  // fp8 keys widened by the converter: the tile's scales ride in its stage
+  L.stage_bytes = conv ? kFp8StageAlloc : (q8 ? kFp8StageBytes : kTileBytes);
   L.a_stages = conv ? kFp8ConvStages : 0;
-  const int ring = conv ? kScaleRing * kBM * 4 : 0;
-  const int tail = N * 256 + ring + (2 * 8 + 2 * kFp8ConvStages + kScaleRing + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
+  const int qbytes = N * (q8 ? 128 : 256);         // q: N rows of D elements
+  const int nring = conv ? kScaleRing : (q8 ? kQ8Ring : 0);
+  const int ring = nring * kBM * 4;
+  const int tail = qbytes + ring + (2 * 8 + 2 * kFp8ConvStages + nring + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
                    8 * (groups + 1) + (fused ? 16 + 4 * kFuseWords : 0);
   int st = ((lean ? kLeanSmem : kMaxSmem) - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
-  L.stages = st > 8 ? 8 : st;
+  L.stages = st > 8 ? 8 : st;  // <= kQ8Ring - 2
   L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
   L.b_off = L.a_off + L.a_stages * kTileBytes;
-  L.ring_off = L.b_off + N * 256;      // fp8 only: per-tile key scales
+  L.ring_off = L.b_off + qbytes;       // fp8 only: per-tile key scales
   L.bar_off = L.ring_off + ring;
-  const int nbars = 2 * L.stages + 2 * L.a_stages + (conv ? kScaleRing : 0) + 2 + 2 + 4;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + nring + 2 + 2 + 4;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4 + 16;   // pref[G + 1], gmax[G]
@@ -421,9 +428,9 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
   uint64_t* empty = full + kStages;
   uint64_t* afull = empty + kStages;          // fp8: converter -> MMA
   uint64_t* aempty = afull + kAStages;        // fp8: MMA -> converter
-  uint64_t* sfull = aempty + kAStages;        // fp8: converter -> epilogue, one per scale slot
-  uint64_t* tfull = sfull + (CONV ? kScaleRing : 0);
-  float* scale_ring = reinterpret_cast<float*>(smem + L.ring_off);  // fp8: [kScaleRing][128]
+  uint64_t* sfull = aempty + kAStages;        // fp8: scales of a tile ready, one per scale slot
+  uint64_t* tfull = sfull + (CONV ? kScaleRing : (Q8 ? kQ8Ring : 0));
+  float* scale_ring = reinterpret_cast<float*>(smem + L.ring_off);  // fp8: [slots][128]
   uint64_t* tempty = tfull + 2;
   uint64_t* qfull = tempty + 2;
   uint64_t* qempty = qfull + 1;
@@ -448,9 +455,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
-      // freed by the converter (widened keys), or by the MMA and - fp8 q: the
-      // epilogue reads each key's scale from the stage - every epilogue thread
-      ptx::mbar_init(&empty[s], CONV ? R::kConvThreads : (Q8 ? 1 + kEpiThreads : 1));
+      // freed by the converter (widened keys), or by the MMA
+      ptx::mbar_init(&empty[s], CONV ? R::kConvThreads : 1);
     }
     for (int s = 0; s < kAStages; ++s) {
       ptx::mbar_init(&afull[s], R::kConvThreads);
@@ -458,6 +464,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     }
     if (CONV)
       for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], kBM);
+    if (Q8)
+      for (int s = 0; s < kQ8Ring; ++s) ptx::mbar_init(&sfull[s], 1);
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull[a], 1);
       ptx::mbar_init(&tempty[a], kEpiThreads);
@@ -621,6 +629,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     int qg = -1;
     uint32_t q_loads = 0;
     uint32_t filled_mask = 0, last_phase_bits = 0;
+    uint32_t sfilled_mask = 0, s_last_phase_bits = 0;  // fp8 q: scale slots with copies issued
     bool ok = true;
     bool released = !fast;  // fast schedule: `setup` not yet arrived on by this warp
     const int32_t* cur_e = t_begin < t_end ? lane_entry(t_begin) : nullptr;
@@ -659,8 +668,16 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         }
         ok = wait_phase(&empty[stage], phase ^ 1u, abort_flag, p.fault);
         if (!ok) break;
-        if (lane == 0)
-          ptx::mbar_arrive_expect_tx(&full[stage], nbox * box_bytes + (FP8 ? nbox * p.box_rows * 4u : 0u));
+        // fp8 q: the tile's scale slot.  It is free: the stage wait above means
+        // the MMA of tile rel - kStages is done, so the epilogue has released
+        // the accumulator of tile rel - kStages - 2 and read every scale up to
+        // that tile, and rel - kQ8Ring <= rel - kStages - 2.
+        const int rel = t - t_begin;
+        const int slot = Q8 ? rel % kQ8Ring : 0;
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(&full[stage], nbox * box_bytes + (CONV ? nbox * p.box_rows * 4u : 0u));
+          if (Q8) ptx::mbar_arrive_expect_tx(&sfull[slot], nbox * p.box_rows * 4u);
+        }
         __syncwarp();
         if ((lane >> bsh) == i && cur_e != nullptr) {
           const int32_t pg = cur < 0 ? 0 : (cur >= p.num_pages ? p.num_pages - 1 : cur);  // clamp: no fault
@@ -669,11 +686,17 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
           uint8_t* dst = S + stage * L.stage_bytes + (uint32_t)box * (uint32_t)p.box_rows * (FP8 ? 128u : 256u);
           if (FP8) ptx::tma_load_3d(dst, &kv_map, 0, y, pg, &full[stage], policy);
           else ptx::tma_load_5d(dst, &kv_map, 0, 0, 0, y >> 3, pg, &full[stage], policy);
-          if (FP8)  // the box's scales land after the key rows of the stage (plain bulk copy:
-                    // 16-byte aligned source, destination and size)
+          // the box's scales (plain bulk copy: 16-byte aligned source,
+          // destination and size) land after the key rows of the stage for
+          // the converter, in the tile's scale slot with fp8 q
+          if (CONV)
             ptx::bulk_load(S + stage * L.stage_bytes + kFp8StageBytes + box * p.box_rows * 4,
                            p.scales + (int64_t)pg * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
                            &full[stage], policy);
+          if (Q8)
+            ptx::bulk_load(scale_ring + slot * kBM + box * p.box_rows,
+                           p.scales + (int64_t)pg * p.scale_stride + (int64_t)y * 4, (uint32_t)p.box_rows * 4u,
+                           &sfull[slot], policy);
         }
         if (!released) {
           __syncwarp();
@@ -682,6 +705,10 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         }
         filled_mask |= 1u << stage;
         last_phase_bits = (last_phase_bits & ~(1u << stage)) | (phase << stage);
+        if (Q8) {
+          sfilled_mask |= 1u << slot;
+          s_last_phase_bits = (s_last_phase_bits & ~(1u << slot)) | ((uint32_t)((rel / kQ8Ring) & 1) << slot);
+        }
         if (++stage == kStages) {
           stage = 0;
           phase ^= 1u;
@@ -697,6 +724,12 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         if (filled_mask & (1u << s)) {
           const long long t0 = clock64();
           while (!ptx::mbar_try_wait(&full[s], (last_phase_bits >> s) & 1u) && clock64() - t0 < kSpinCycles) {
+          }
+        }
+      for (int s = 0; Q8 && s < kQ8Ring; ++s)
+        if (sfilled_mask & (1u << s)) {
+          const long long t0 = clock64();
+          while (!ptx::mbar_try_wait(&sfull[s], (s_last_phase_bits >> s) & 1u) && clock64() - t0 < kSpinCycles) {
           }
         }
     }
@@ -832,15 +865,12 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       } else if (Q8) {
-        // the scale sits in the tile's TMA stage, which stays filled until this
-        // thread (and the MMA) release it; waiting on its completed fill orders
-        // the copied bytes for this thread
+        // the tile's scales, copied into their slot of the scale ring;
+        // waiting on the slot's completed fill orders the copied bytes
         const int i = t - t_begin;
-        const int st = i % kStages;
-        ok = wait_phase(&full[st], (uint32_t)(i / kStages) & 1u, abort_flag, p.fault);
+        ok = wait_phase(&sfull[i % kQ8Ring], (uint32_t)(i / kQ8Ring) & 1u, abort_flag, p.fault);
         if (!ok) continue;
-        const float sc = *reinterpret_cast<const float*>(S + st * L.stage_bytes + kFp8StageBytes + m * 4);
-        ptx::mbar_arrive(&empty[st]);
+        const float sc = scale_ring[(i % kQ8Ring) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
@@ -869,7 +899,12 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
           for (int rr = 0; rr < kRowsPerUnit; ++rr) {
             const int j = u * kRowsPerUnit + rr;
             if (j >= nr) break;
-            float part = 0.0f;
+            // the head sum: with 16 or more heads, four partial sums (heads
+            // h, h + 4, ... in each) so the dependent chain is H / 4 long
+            constexpr int kParts = H >= 16 ? 4 : 1;
+            float parts[kParts];
+#pragma unroll
+            for (int u = 0; u < kParts; ++u) parts[u] = 0.0f;
 #pragma unroll
             for (int h = 0; h < H; ++h) {
               // weights of row j: four at a time when H is a multiple of 4
@@ -882,8 +917,10 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
               }
               const uint32_t x = H < 16 ? v[q][rr * H + h] : v[q * kLdPerUnit + h / 16][h % 16];
               const float xv = FP8 ? sgn * __uint_as_float(x) : __uint_as_float(x);
-              part = fmaf(wh, relu_nan(xv), part);
+              parts[h % kParts] = fmaf(wh, relu_nan(xv), parts[h % kParts]);
             }
+            float part = parts[0];
+            if (kParts == 4) part = (parts[0] + parts[1]) + (parts[2] + parts[3]);
             if (FP8) part *= mag;
             float* const dst = obu + (int64_t)rr * oc;
             if (unmasked) {
