@@ -87,6 +87,12 @@ __device__ __forceinline__ void tma_load_5d(void* dst, const CUtensorMap* m, int
       : "memory");
 }
 
+// L2 prefetch of `bytes` contiguous bytes (16-byte aligned, a multiple of 16):
+// a cache hint, with no effect on the values any load returns.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Plain (untensored) bulk copy global -> shared; sizes and addresses 16-byte aligned.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {

@@ -32,6 +32,7 @@ struct TopkArgs {
   int32_t cap;   // cached columns per CTA (multiple of 4, <= kCacheMax)
   int32_t cpw;   // candidate list entries per warp (multiple of 4)
   int32_t bulk;  // segments start 16-byte aligned: bulk copies fill the cache
+  int32_t pcap;  // candidates of the sampled-pivot path (0: off)
 };
 
 template <bool CLUSTER>
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
   ptx::grid_dep_wait();
   ptx::grid_dep_launch();
   const RowTask task{a.logits + row * a.row_stride, n, a.out + row * (int64_t)a.k};
-  const Config cf{a.k, a.cap, a.cpw, a.bulk, a.fault};
+  const Config cf{a.k, a.cap, a.cpw, a.bulk, a.fault, a.pcap};
   select_row<kT, CLUSTER, false, kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh, CL, rank);
 }
 
@@ -183,6 +184,9 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   a.k = k;
   a.cap = (int32_t)pl.cap;
   a.cpw = (int32_t)pl.cpw;
+  // the sampled-pivot path's candidates (key and column each) after its histograms
+  const int64_t pc = ((int64_t)pl.smem / 4 - kRegHistWords) / 2;
+  a.pcap = (int32_t)((pc < kT * kRegKeys ? pc : kT * kRegKeys) & ~int64_t(3));
   // segment starts are multiples of 4 columns: 16-byte aligned when rows are
   a.bulk = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (row_stride & 3) == 0;
   cudaLaunchConfig_t cfg = {};

@@ -79,6 +79,7 @@ struct Config {
   int cpw;    // candidate list entries per warp (multiple of 4)
   int bulk;   // segments start 16-byte aligned: bulk copies fill the cache
   unsigned int* fault;  // bit 1 set when a copy wait gives up
+  int pcap;   // candidates the sampled-pivot path holds (<= NT * KPT; below k: path off)
 };
 
 // Dynamic shared memory one selecting CTA needs (bytes).
@@ -269,9 +270,14 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* hist, uint32_t* acc,
 // a cluster the per-digit accumulators (kAccWords).
 constexpr int kRegHistWords = 2 * kBins + 1024;
 
-template <int NT, int KPT, bool COHERENT, bool CLUSTER>
+// CAND: the keys are the n candidates of the sampled-pivot path, already keys,
+// in the per-warp slices of `wcap` entries of ckey / ccol; slice w holds the
+// candidates from order position sh.weq[w] on (order = column order).  The
+// selected columns are the candidates' ccol entries.
+template <int NT, int KPT, bool COHERENT, bool CLUSTER, bool CAND = false>
 __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh,
-                                               int C, int part) {
+                                               int C, int part, const uint32_t* ckey = nullptr,
+                                               const int32_t* ccol = nullptr, int wcap = 0) {
   static_assert(KPT % 4 == 0, "keys per thread in groups of 4");
   const int tid = (int)threadIdx.x;
   const int lane = lane_id();
@@ -294,7 +300,31 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
   const int c0 = tid * q;
   const int mine = max(0, min(q, len - c0));  // valid keys of this thread
   uint32_t key[KPT];
-  if ((q & 3) == 0 && (reinterpret_cast<uintptr_t>(x + c0) & 15u) == 0) {
+  int cidx[CAND ? KPT : 1];  // CAND: slice index of each of this thread's candidates
+  if (CAND) {
+    // the slice w holding order position g: [lo, hi) = [weq[w], weq[w + 1])
+    constexpr int kWs = NT / 32;
+    int w = 0, lo = 0, hi = kWs > 1 ? sh.weq[1] : INT32_MAX;
+    while (c0 >= hi && w + 1 < kWs) {
+      ++w;
+      lo = hi;
+      hi = w + 1 < kWs ? sh.weq[w + 1] : INT32_MAX;
+    }
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      cidx[j] = 0;
+      key[j] = 0u;
+      if (j < mine) {
+        while (c0 + j >= hi && w + 1 < kWs) {
+          ++w;
+          lo = hi;
+          hi = w + 1 < kWs ? sh.weq[w + 1] : INT32_MAX;
+        }
+        cidx[j] = w * wcap + (c0 + j - lo);
+        key[j] = ckey[cidx[j]];
+      }
+    }
+  } else if ((q & 3) == 0 && (reinterpret_cast<uintptr_t>(x + c0) & 15u) == 0) {
 #pragma unroll
     for (int j = 0; j < KPT; j += 4) {
       uint4 kk = make_uint4(0u, 0u, 0u, 0u);
@@ -400,7 +430,7 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
     const bool take = (j < mine && key[j] > thr) || (is_eq && eq_rank < remaining);
     eq_rank += (int)is_eq;
     if (take) {
-      if (pos < k) o[pos] = s0 + c0 + j;
+      if (pos < k) o[pos] = CAND ? ccol[cidx[CAND ? j : 0]] : s0 + c0 + j;
       ++pos;
     }
   }
@@ -409,6 +439,175 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
     __syncwarp();
     cluster_wait();
   }
+}
+
+// ---- sampled-pivot selection -------------------------------------------------
+// A row one CTA selects alone, longer than its keys-in-registers limit, with
+// k well below its length (the long prefill and MTP rows):
+//  1. A sample - every 8th block of 128 columns, or sparser for rows so long
+//     that the sample would not fit the candidate slices - gives a threshold T below
+//     the row's k-th largest key with a wide margin: the lower edge of the
+//     22-bit key bin holding the sample's j-th largest key, j the k-th
+//     place scaled to the sample plus four standard deviations and 16.
+//  2. One pass over the row (each warp a contiguous segment, four 128-column
+//     steps of loads in flight) writes the columns at or above T, with their
+//     keys, into the warp's own slice of shared memory, in column order.
+//  3. The exact selection runs on the candidates alone, keys in registers
+//     (select_row_reg reading the warps' slices in order), and writes the
+//     selected candidates' columns.
+// It gives up - the caller then runs the full path - when fewer than k
+// columns reach T (every selected key must be a candidate) or a warp's slice
+// overflows; the decisions read shared values, so every thread takes the
+// same one.  Shared memory at `dyn`: the three histograms (kRegHistWords),
+// then per warp `wcap` candidate keys, then per warp `wcap` columns.
+
+// The smallest float whose key (topk_key) is at least tk, for the compare
+// x >= T on floats: -inf below every finite key, NaN above them (no float
+// compares >= NaN).
+__device__ __forceinline__ float key_floor_float(uint32_t tk) {
+  if (tk <= 0x007FFFFFu) return -INFINITY;
+  if (tk & 0x80000000u) return __uint_as_float(tk & 0x7FFFFFFFu);
+  return __uint_as_float(~tk);
+}
+
+constexpr int kSampleEvery = 8;  // sampled blocks of kSeg columns: one in kSampleEvery
+constexpr int kPivotSteps = 8;   // 128-column steps a warp loads at once
+
+template <int NT, bool COHERENT, int KPT>
+__device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh) {
+  constexpr int kW = NT / 32;
+  const int tid = (int)threadIdx.x, lane = lane_id(), warp = tid >> 5;
+  const int n = task.n, k = cf.k;
+  const int wcap = (cf.pcap / kW) & ~3;  // candidate slots of a warp
+  const float* x = task.row;
+  const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+  uint32_t* h0 = dyn;
+  uint32_t* h1 = h0 + kBins;
+  uint32_t* skey = dyn + kRegHistWords + warp * wcap;  // this warp's slice
+  int32_t* scol = reinterpret_cast<int32_t*>(dyn + kRegHistWords + kW * wcap) + warp * wcap;
+  // four columns c..c+3 (c a multiple of 4) up to `end`; past it NaN, which
+  // compares false with every threshold
+  auto load4 = [&](int c, int end) -> float4 {
+    if (vec && c + 4 <= end) return ld_row4<COHERENT>(x + c);
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = c + u < end ? ld_row1<COHERENT>(x + c + u) : __uint_as_float(0x7FC00000u);
+    return make_float4(v[0], v[1], v[2], v[3]);
+  };
+  const int nblk = (n + kSeg - 1) / kSeg;
+  // one block in `every` (more than kSampleEvery for rows whose sample would
+  // not fit the candidate slices, where it is kept)
+  const int maxblk = max(1, kW * wcap / kSeg);
+  const int every = max(kSampleEvery, (nblk + maxblk - 1) / maxblk);
+  const int nsb = (nblk + every - 1) / every;  // sampled blocks
+  const int last = (nsb - 1) * every;
+  const int S = (nsb - 1) * kSeg + min(kSeg, n - last * kSeg);  // sampled columns
+  const double r = (double)k * S / n;
+  const int64_t jj = (int64_t)ceil(r + 4.0 * sqrt(r) + 16.0);
+  if (jj > S || wcap < 4) return false;  // nothing written yet; the same in every thread
+  const int j = (int)jj;
+  // the whole row streams into L2 at once (16 KB bulk prefetches of its
+  // 16-byte aligned part) while the sample is read; both passes then read L2
+  if (tid == 0 && vec) {
+    const int n4 = n & ~3;
+    for (int c = 0; c < n4; c += kChunk) ptx::bulk_prefetch_l2(x + c, 4u * (uint32_t)min(kChunk, n4 - c));
+  }
+  for (int i = tid; i < 2 * kBins; i += NT) h0[i] = 0;
+  bar_sync<NT>();  // histograms zeroed
+  // (1) sample histogram of the top 11 bits (warp w takes sampled blocks w,
+  // w + kW, ... four at a time; the keys stay in shared memory, in the
+  // candidate slices the main pass fills later), then of the next 11 in d0's
+  // bin from the kept keys
+  uint32_t* skeep = dyn + kRegHistWords;  // sample key i at skeep[i]: block i / kSeg, column 4 lane + e
+  for (int b0 = warp * every; b0 < nblk; b0 += 4 * kW * every) {
+    float4 f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b = b0 + u * kW * every;
+      f[u] = b < nblk ? load4(b * kSeg + 4 * lane, n) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int b = b0 + u * kW * every;
+      if (b >= nblk) break;
+      const int c = b * kSeg + 4 * lane;
+      const uint4 kk = keys4(f[u]);
+      *reinterpret_cast<uint4*>(skeep + (b / every) * kSeg + 4 * lane) = kk;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (c + e < n) atomicAdd(&h0[lane_of(kk, e) >> 21], 1u);
+    }
+  }
+  bar_sync<NT>();
+  find_digit<NT>(sh, h0, kBins, j);
+  bar_sync<NT>();
+  const uint32_t d0 = (uint32_t)sh.digit;
+  const int j1 = j - sh.above;
+  for (int i = tid; i < nsb * kSeg; i += NT) {
+    const int c = (i / kSeg) * every * kSeg + (i % kSeg);  // the row column of sample key i
+    const uint32_t key = skeep[i];
+    if (c < n && (key >> 21) == d0) atomicAdd(&h1[(key >> 10) & 2047u], 1u);
+  }
+  bar_sync<NT>();
+  find_digit<NT>(sh, h1, kBins, j1);
+  bar_sync<NT>();
+  const float T = key_floor_float((d0 << 21) | ((uint32_t)sh.digit << 10));
+  // (2) the columns >= T, per warp in column order
+  const unsigned lt = (1u << lane) - 1u;
+  const int wseg = (n + kW * kSeg - 1) / (kW * kSeg) * kSeg;
+  const int w0 = min(n, warp * wseg), w1 = min(n, w0 + wseg);
+  int ncw = 0;  // this warp's candidates (warp-uniform)
+  for (int c0 = w0; c0 < w1; c0 += kPivotSteps * kSeg) {  // warp-uniform trip count
+    float4 f[kPivotSteps];
+#pragma unroll
+    for (int u = 0; u < kPivotSteps; ++u) f[u] = load4(c0 + u * kSeg + 4 * lane, w1);
+#pragma unroll
+    for (int u = 0; u < kPivotSteps; ++u) {
+      const int c = c0 + u * kSeg + 4 * lane;
+      const bool b0 = f[u].x >= T, b1 = f[u].y >= T, b2 = f[u].z >= T, b3 = f[u].w >= T;
+      // column order is lane-major: the candidates of the lanes below this one
+      // come first, counted from one ballot per key slot
+      const unsigned v0 = __ballot_sync(0xFFFFFFFFu, b0), v1 = __ballot_sync(0xFFFFFFFFu, b1);
+      const unsigned v2 = __ballot_sync(0xFFFFFFFFu, b2), v3 = __ballot_sync(0xFFFFFFFFu, b3);
+      int pos = ncw + __popc(v0 & lt) + __popc(v1 & lt) + __popc(v2 & lt) + __popc(v3 & lt);
+      if (b0) {
+        if (pos < wcap) { scol[pos] = c; skey[pos] = topk_key(f[u].x); }
+        ++pos;
+      }
+      if (b1) {
+        if (pos < wcap) { scol[pos] = c + 1; skey[pos] = topk_key(f[u].y); }
+        ++pos;
+      }
+      if (b2) {
+        if (pos < wcap) { scol[pos] = c + 2; skey[pos] = topk_key(f[u].z); }
+        ++pos;
+      }
+      if (b3 && pos < wcap) { scol[pos] = c + 3; skey[pos] = topk_key(f[u].w); }
+      ncw += __popc(v0) + __popc(v1) + __popc(v2) + __popc(v3);
+    }
+  }
+  if (lane == 0) sh.wgt[warp] = ncw;
+  bar_sync<NT>();
+  // exclusive prefix of the warps' counts (every warp computes it), the total
+  int wc = lane < kW ? sh.wgt[lane] : 0, wi = wc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+    if (lane >= o) wi += t;
+  }
+  const int M = __shfl_sync(0xFFFFFFFFu, wi, 31);
+  const bool over = __any_sync(0xFFFFFFFFu, wc > wcap);
+  if (warp == 0 && lane < kW) sh.weq[lane] = wi - wc;  // slice base of warp `lane` in the candidate order
+  bar_sync<NT>();
+  if (M < k || over) return false;  // every thread has read the counts (barrier above)
+  const RowTask ctask{task.row, M, task.out};
+  const uint32_t* ck = dyn + kRegHistWords;
+  const int32_t* cc = reinterpret_cast<const int32_t*>(dyn + kRegHistWords + kW * wcap);
+  if (KPT > 8 && M <= NT * 8)  // the same in every thread
+    select_row_reg<NT, (KPT > 8 ? 8 : KPT), COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, ck, cc, wcap);
+  else
+    select_row_reg<NT, KPT, COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, ck, cc, wcap);
+  return true;
 }
 
 // Selects one row.  Called by threads [0, NT) of the CTA (every one of them,
@@ -460,6 +659,8 @@ __device__ __forceinline__ void select_row(const RowTask& task, const Config& cf
       select_row_reg<NT, K4, COHERENT, CLUSTER>(task, cf, dyn, sh, CL, rank);
       return;
     }
+    // one CTA, a longer row: the sampled pivot, unless it gives up
+    if (!multi && cf.pcap >= cf.k && select_row_pivot<NT, COHERENT, K4>(task, cf, dyn, sh)) return;
   }
   const int C = multi ? CL : 1;
   const int part = multi ? rank : 0;

@@ -255,7 +255,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   const Layout L = make_layout(N, up.num_groups, kind, fuse != nullptr, lean);
   up.topk_out = nullptr;
   up.fuse_sync = nullptr;
-  up.topk_k = up.topk_cap = up.topk_cpw = 0;
+  up.topk_k = up.topk_cap = up.topk_cpw = up.topk_pcap = 0;
   if (fuse) {
     if (up.num_groups > kFuseMaxGroups) {
       *msg = "too many row groups for the fused selection";
@@ -277,6 +277,10 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
     up.topk_k = fuse->k;
     up.topk_cap = (int32_t)cap;
     up.topk_cpw = cpw;
+    // the sampled-pivot path's candidates (key and column each) after its histograms
+    const int64_t pc = (((int64_t)L.bar_off - kSelSharedBytes) / 4 - sel::kRegHistWords) / 2;
+    const int64_t pmax = (int64_t)nt * kFuseKeys;
+    up.topk_pcap = (int32_t)((pc < pmax ? pc : pmax) & ~int64_t(3));
     if (kind == kKindFp8Q) return launch_q8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);
     return p.fp8 ? launch_fp8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream)
                  : launch_bf16_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);

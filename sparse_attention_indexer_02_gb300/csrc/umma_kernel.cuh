@@ -117,7 +117,7 @@ struct UmmaParams {
   // fused selection (kernels instantiated with FUSE only)
   int32_t* topk_out;    // [num_rows][topk_k] selected columns
   uint32_t* fuse_sync;  // caller workspace: done[G] | cursor[G] | finished; zero between calls
-  int32_t topk_k, topk_cap, topk_cpw;
+  int32_t topk_k, topk_cap, topk_cpw, topk_pcap;
 };
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-aligned base);
@@ -332,7 +332,7 @@ __device__ __forceinline__ void fused_select(const UmmaParams& p, const int32_t*
   const int k = p.topk_k;
   sel::Shared& sh = *reinterpret_cast<sel::Shared*>(smem);
   uint32_t* dyn = reinterpret_cast<uint32_t*>(smem + kSelSharedBytes);
-  const sel::Config cf{k, p.topk_cap, p.topk_cpw, 0, p.fault};
+  const sel::Config cf{k, p.topk_cap, p.topk_cpw, 0, p.fault, p.topk_pcap};
   uint32_t* done = p.fuse_sync;
   uint32_t* cursor = done + G;
   uint32_t* finished = done + 2 * G;

@@ -529,6 +529,33 @@ def test_topk_threshold_bin_taken_whole(oracle_mod, n):
     assert sorted(idx[0].tolist()) == np.flatnonzero(x[0] >= 1.0).tolist()
 
 
+@pytest.mark.parametrize("rows,n", [(4, 16000), (200, 22528), (160, 65537)])
+def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
+    """Rows one CTA selects alone and longer than its keys-in-registers limit
+    (4 rows of 16000 columns, 200 of 22528, 160 of 65537 - sampled more
+    sparsely): a sample of every 8th block of 128 columns sets a threshold, the
+    exact selection runs on the candidates above it.  Continuous values, then every sampled block raised far above
+    the rest (the sample's threshold lets fewer than k columns through, so the
+    full path must take over), then exact zeros spanning the k-th place (the
+    lowest zero columns win)."""
+    k = 2048
+    rng = np.random.default_rng(rows)
+    vis = np.full(rows, n, np.int32)
+    vis[1] = n - 123
+    base = qi.random_logit_rows(rng, rows, n, vis, zero_frac=0.0)
+    high = base.copy()
+    blk = np.arange(n) // 128
+    high[:, blk % 8 == 0] += np.float32(10.0)
+    ties = np.where(np.isfinite(base), np.float32(-1.0), base)
+    for r in range(rows):
+        cols = rng.permutation(int(vis[r]))
+        ties[r, cols[:1500]] = 2.0
+        ties[r, cols[1500:4500]] = 0.0
+    for x in (base, high, ties):
+        idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k)
+        assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+
+
 def test_topk_visible_beyond_stride_is_clamped():
     x = np.arange(40, dtype=np.float32).reshape(2, 20)
     xt = torch.from_numpy(x).cuda()
