@@ -556,6 +556,21 @@ def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
         assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
 
 
+def test_topk_more_rows_than_resident_ctas(oracle_mod):
+    """More rows than the device holds CTAs at once, mixing every path a row
+    can take: at most k columns, keys in registers, the sampled pivot, and
+    its fallback (all values equal)."""
+    rows, width, k = 700, 12000, 1024
+    rng = np.random.default_rng(700)
+    vis = rng.integers(9000, width + 1, size=rows).astype(np.int32)
+    vis[::7] = rng.integers(0, k + 1, size=vis[::7].shape)      # fit in k
+    vis[3::7] = rng.integers(k + 1, 8192, size=vis[3::7].shape)  # registers
+    x = qi.random_logit_rows(rng, rows, width, vis, zero_frac=0.05)
+    x[5::50, :] = np.where(np.isfinite(x[5::50, :]), np.float32(0.75), x[5::50, :])  # all equal
+    idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+
+
 def test_topk_visible_beyond_stride_is_clamped():
     x = np.arange(40, dtype=np.float32).reshape(2, 20)
     xt = torch.from_numpy(x).cuda()
