@@ -79,7 +79,7 @@ struct Config {
   int cpw;    // candidate list entries per warp (multiple of 4)
   int bulk;   // segments start 16-byte aligned: bulk copies fill the cache
   unsigned int* fault;  // bit 1 set when a copy wait gives up
-  int pcap;   // candidates the sampled-pivot path holds (<= NT * KPT; below k: path off)
+  int pcap;   // candidate columns the sampled-pivot path holds (<= NT * KPT; below k: path off)
 };
 
 // Dynamic shared memory one selecting CTA needs (bytes).
@@ -270,14 +270,14 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* hist, uint32_t* acc,
 // a cluster the per-digit accumulators (kAccWords).
 constexpr int kRegHistWords = 2 * kBins + 1024;
 
-// CAND: the keys are the n candidates of the sampled-pivot path, already keys,
-// in the per-warp slices of `wcap` entries of ckey / ccol; slice w holds the
-// candidates from order position sh.weq[w] on (order = column order).  The
-// selected columns are the candidates' ccol entries.
+// CAND: the n keys are those of the sampled-pivot path's candidates, whose
+// columns are in the per-warp slices of `wcap` entries of ccol; slice w holds
+// the candidates from order position sh.weq[w] on (order = column order).
+// Their logits are read again from the row; the selected columns are the
+// candidates' ccol entries.
 template <int NT, int KPT, bool COHERENT, bool CLUSTER, bool CAND = false>
 __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh,
-                                               int C, int part, const uint32_t* ckey = nullptr,
-                                               const int32_t* ccol = nullptr, int wcap = 0) {
+                                               int C, int part, const int32_t* ccol = nullptr, int wcap = 0) {
   static_assert(KPT % 4 == 0, "keys per thread in groups of 4");
   const int tid = (int)threadIdx.x;
   const int lane = lane_id();
@@ -313,7 +313,6 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
 #pragma unroll
     for (int j = 0; j < KPT; ++j) {
       cidx[j] = 0;
-      key[j] = 0u;
       if (j < mine) {
         while (c0 + j >= hi && w + 1 < kWs) {
           ++w;
@@ -321,9 +320,14 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
           hi = w + 1 < kWs ? sh.weq[w + 1] : INT32_MAX;
         }
         cidx[j] = w * wcap + (c0 + j - lo);
-        key[j] = ckey[cidx[j]];
       }
     }
+    // then every logit load at once (independent of one another)
+    float v[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) v[j] = j < mine ? ld_row1<COHERENT>(task.row + ccol[cidx[j]]) : 0.0f;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) key[j] = j < mine ? topk_key(v[j]) : 0u;
   } else if ((q & 3) == 0 && (reinterpret_cast<uintptr_t>(x + c0) & 15u) == 0) {
 #pragma unroll
     for (int j = 0; j < KPT; j += 4) {
@@ -449,17 +453,18 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
 //     the row's k-th largest key with a wide margin: the lower edge of the
 //     22-bit key bin holding the sample's j-th largest key, j the k-th
 //     place scaled to the sample plus four standard deviations and 16.
-//  2. One pass over the row (each warp a contiguous segment, four 128-column
-//     steps of loads in flight) writes the columns at or above T, with their
-//     keys, into the warp's own slice of shared memory, in column order.
+//  2. One pass over the row (each warp a contiguous segment, each lane 16
+//     consecutive columns a step) writes the columns at or above T into the
+//     warp's own slice of shared memory, in column order (a lane's offset
+//     from one scan of its candidate count, its stores one per set bit).
 //  3. The exact selection runs on the candidates alone, keys in registers
-//     (select_row_reg reading the warps' slices in order), and writes the
-//     selected candidates' columns.
+//     (select_row_reg reading the warps' slices in order, each candidate's
+//     logit again from L2), and writes the selected candidates' columns.
 // It gives up - the caller then runs the full path - when fewer than k
 // columns reach T (every selected key must be a candidate) or a warp's slice
 // overflows; the decisions read shared values, so every thread takes the
 // same one.  Shared memory at `dyn`: the three histograms (kRegHistWords),
-// then per warp `wcap` candidate keys, then per warp `wcap` columns.
+// then per warp `wcap` candidate columns.
 
 // The smallest float whose key (topk_key) is at least tk, for the compare
 // x >= T on floats: -inf below every finite key, NaN above them (no float
@@ -471,7 +476,7 @@ __device__ __forceinline__ float key_floor_float(uint32_t tk) {
 }
 
 constexpr int kSampleEvery = 8;  // sampled blocks of kSeg columns: one in kSampleEvery
-constexpr int kPivotSteps = 8;   // 128-column steps a warp loads at once
+constexpr int kLaneCols = 16;    // consecutive columns a lane covers per step of the pivot pass
 
 template <int NT, bool COHERENT, int KPT>
 __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh) {
@@ -483,8 +488,7 @@ __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Conf
   const bool vec = (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
   uint32_t* h0 = dyn;
   uint32_t* h1 = h0 + kBins;
-  uint32_t* skey = dyn + kRegHistWords + warp * wcap;  // this warp's slice
-  int32_t* scol = reinterpret_cast<int32_t*>(dyn + kRegHistWords + kW * wcap) + warp * wcap;
+  int32_t* scol = reinterpret_cast<int32_t*>(dyn + kRegHistWords) + warp * wcap;  // this warp's slice
   // four columns c..c+3 (c a multiple of 4) up to `end`; past it NaN, which
   // compares false with every threshold
   auto load4 = [&](int c, int end) -> float4 {
@@ -553,38 +557,35 @@ __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Conf
   bar_sync<NT>();
   const float T = key_floor_float((d0 << 21) | ((uint32_t)sh.digit << 10));
   // (2) the columns >= T, per warp in column order
-  const unsigned lt = (1u << lane) - 1u;
-  const int wseg = (n + kW * kSeg - 1) / (kW * kSeg) * kSeg;
+  constexpr int kWarpStep = 32 * kLaneCols;
+  const int wseg = (n + kW * kWarpStep - 1) / (kW * kWarpStep) * kWarpStep;
   const int w0 = min(n, warp * wseg), w1 = min(n, w0 + wseg);
   int ncw = 0;  // this warp's candidates (warp-uniform)
-  for (int c0 = w0; c0 < w1; c0 += kPivotSteps * kSeg) {  // warp-uniform trip count
-    float4 f[kPivotSteps];
+  for (int c0 = w0; c0 < w1; c0 += kWarpStep) {  // warp-uniform trip count
+    const int c = c0 + kLaneCols * lane;
+    float4 f[kLaneCols / 4];
 #pragma unroll
-    for (int u = 0; u < kPivotSteps; ++u) f[u] = load4(c0 + u * kSeg + 4 * lane, w1);
+    for (int u = 0; u < kLaneCols / 4; ++u) f[u] = load4(c + 4 * u, w1);
+    uint32_t m = 0;  // bit i: column c + i is a candidate
 #pragma unroll
-    for (int u = 0; u < kPivotSteps; ++u) {
-      const int c = c0 + u * kSeg + 4 * lane;
-      const bool b0 = f[u].x >= T, b1 = f[u].y >= T, b2 = f[u].z >= T, b3 = f[u].w >= T;
-      // column order is lane-major: the candidates of the lanes below this one
-      // come first, counted from one ballot per key slot
-      const unsigned v0 = __ballot_sync(0xFFFFFFFFu, b0), v1 = __ballot_sync(0xFFFFFFFFu, b1);
-      const unsigned v2 = __ballot_sync(0xFFFFFFFFu, b2), v3 = __ballot_sync(0xFFFFFFFFu, b3);
-      int pos = ncw + __popc(v0 & lt) + __popc(v1 & lt) + __popc(v2 & lt) + __popc(v3 & lt);
-      if (b0) {
-        if (pos < wcap) { scol[pos] = c; skey[pos] = topk_key(f[u].x); }
-        ++pos;
-      }
-      if (b1) {
-        if (pos < wcap) { scol[pos] = c + 1; skey[pos] = topk_key(f[u].y); }
-        ++pos;
-      }
-      if (b2) {
-        if (pos < wcap) { scol[pos] = c + 2; skey[pos] = topk_key(f[u].z); }
-        ++pos;
-      }
-      if (b3 && pos < wcap) { scol[pos] = c + 3; skey[pos] = topk_key(f[u].w); }
-      ncw += __popc(v0) + __popc(v1) + __popc(v2) + __popc(v3);
+    for (int u = 0; u < kLaneCols / 4; ++u)
+      m |= (uint32_t)(f[u].x >= T) << (4 * u) | (uint32_t)(f[u].y >= T) << (4 * u + 1) |
+           (uint32_t)(f[u].z >= T) << (4 * u + 2) | (uint32_t)(f[u].w >= T) << (4 * u + 3);
+    const int nc = __popc(m);
+    int incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += t;
     }
+    int pos = ncw + incl - nc;
+    while (m) {
+      const int i = __ffs(m) - 1;
+      m &= m - 1u;
+      if (pos < wcap) scol[pos] = c + i;
+      ++pos;
+    }
+    ncw += __shfl_sync(0xFFFFFFFFu, incl, 31);
   }
   if (lane == 0) sh.wgt[warp] = ncw;
   bar_sync<NT>();
@@ -601,12 +602,11 @@ __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Conf
   bar_sync<NT>();
   if (M < k || over) return false;  // every thread has read the counts (barrier above)
   const RowTask ctask{task.row, M, task.out};
-  const uint32_t* ck = dyn + kRegHistWords;
-  const int32_t* cc = reinterpret_cast<const int32_t*>(dyn + kRegHistWords + kW * wcap);
+  const int32_t* cc = reinterpret_cast<const int32_t*>(dyn + kRegHistWords);
   if (KPT > 8 && M <= NT * 8)  // the same in every thread
-    select_row_reg<NT, (KPT > 8 ? 8 : KPT), COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, ck, cc, wcap);
+    select_row_reg<NT, (KPT > 8 ? 8 : KPT), COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, cc, wcap);
   else
-    select_row_reg<NT, KPT, COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, ck, cc, wcap);
+    select_row_reg<NT, KPT, COHERENT, false, true>(ctask, cf, dyn, sh, 1, 0, cc, wcap);
   return true;
 }
 
