@@ -35,13 +35,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 int pick_n(int rows_per_group, int heads) {
   const int need = rows_per_group * heads;
-  for (int n : {16, 32, 64, 128, 256})
+  for (int n : {16, 32, 64, 128, 192, 256})
     if (need <= n) return n;
   return 0;
 }
 
+// Rows a group stacks into the MMA's N (rows x heads <= 256).  A request
+// with more rows than fit takes groups of 192 / H rows: N = 192 is one batch
+// of four units per epilogue warp, three warps a TMEM lane quadrant, where
+// N = 256 gives the quadrant's warps 6, 5 and 5 units (prefill scoring 480 ->
+// 411 us).
 void group_shape(const qsa_paged_desc& d, int* G_rows, int* N) {
-  int g = 256 / d.num_heads;
+  const bool many = (int64_t)d.rows_per_req * d.num_heads > 256;
+  int g = (many ? 192 : 256) / d.num_heads;
   if (g < 1) g = 1;
   if (g > d.rows_per_req) g = d.rows_per_req;
   *G_rows = g;

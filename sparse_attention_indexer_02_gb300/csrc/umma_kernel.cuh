@@ -136,7 +136,8 @@ inline Layout make_layout(int N, int groups, int kind, bool fused = false, bool 
   const bool conv = kind == kKindFp8Keys, q8 = kind == kKindFp8Q;
   Layout L;
   L.n = N;
-  L.tmem_cols = 2 * N < 32 ? 32 : 2 * N;
+  L.tmem_cols = 32;  // two accumulators of N columns, allocated as a power of two
+  while (L.tmem_cols < 2 * N) L.tmem_cols *= 2;
   L.idesc = q8 ? ptx::idesc_e4m3_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N);
   // fp8 keys widened by the converter: the tile's scales ride in its stage
   L.stage_bytes = conv ? kFp8StageAlloc : (q8 ? kFp8StageBytes : kTileBytes);
