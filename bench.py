@@ -2,9 +2,8 @@
 """Benchmark of the QSA-indexer hot path: paged MQA-logits scoring + top-k.
 
 One step = qsa_paged_mqa_logits + qsa_select_topk over one batch of the
-workload (two kernel launches; with --step fused one qsa_paged_mqa_topk call,
-the selection inside the scoring kernel for decode-sized calls).  Prints one
-JSON line.
+workload (two kernel launches; with --step fused one qsa_paged_mqa_topk
+call).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -378,6 +377,8 @@ def build_record():
     return {"ptxas_O0_units": qbuild.o0_units()}
 
 
+FORCED = {"variant": -1}  # the scorer variant --variant forces (-1: the dispatch's)
+
 SWEEP = ["tiny_mtp", "single_row_decode", "mtp3_verify_p16", "mtp3_verify_p64", "mtp3_large_p16",
          "mtp3_large_p64", "fp8_h64", "prefill_chunk", "fp8q_h64", "ragged_nn8"]
 
@@ -491,6 +492,19 @@ class Workload:
             g = self.capture(n, what)
             out[key] = stats(self.time_graph(g, n, reps))
             del g
+        # the one call with the selection inside the scoring kernel (forced;
+        # the dispatch takes the two launches), where that kernel serves the shape
+        qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
+        try:
+            for i in range(3):
+                self.one_call(self.sets[i % self.copies])
+            if qsa.last_variant() == qsa.VARIANT_UMMA_TOPK:
+                torch.cuda.synchronize(self.dev)
+                g = self.capture(n, "one-call")
+                out["fused_kernel_us"] = stats(self.time_graph(g, n, reps))
+                del g
+        finally:
+            qsa.force_variant(FORCED["variant"])
         return out
 
     def summary(self, ks, peaks):
@@ -535,9 +549,9 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     qbuild.build()
     qsa.load_library()
-    if args.variant != "auto":
-        qsa.force_variant({"rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA,
-                           "lean": qsa.VARIANT_UMMA_LEAN}[args.variant])
+    FORCED["variant"] = {"auto": qsa.VARIANT_AUTO, "rowcore": qsa.VARIANT_ROWCORE, "umma": qsa.VARIANT_UMMA,
+                         "lean": qsa.VARIANT_UMMA_LEAN}[args.variant]
+    qsa.force_variant(FORCED["variant"])
     peaks = measured_peaks()
 
     W = Workload(args.workload, dev, rank, rotate=not args.no_rotate)
@@ -690,7 +704,8 @@ def run_gpu(args):
             "us_per_call": score_us, "key_gbs_scoring": head["key_gbs_scoring"],
             "topk_us_per_row": head["topk_us_per_row"], "topk_us_per_call": topk_us,
             "step_us": round(1e3 * ms_step, 3),
-            "fused_step_us": ks["one_call_us"]["median"], "fused_variant": ks["one_call_variant"],
+            "one_call_us": ks["one_call_us"]["median"], "one_call_variant": ks["one_call_variant"],
+            "fused_kernel_us": ks.get("fused_kernel_us", {}).get("median"),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": (1 if form == "one-call" else 2) * K, "clocks": clocks,
             "build": build_record(), "workloads": workloads,

@@ -202,13 +202,15 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
 
 /*
  * qsa_paged_mqa_topk - qsa_paged_mqa_logits_ex and then the top-k of every row,
- * in one call (one kernel for decode-sized calls).
+ * in one call.
  *
  * The pages score and then select in two steps, and vLLM #62589 "Details"
  * notes that the only consumer of the logits, the decode top-k, reads each
- * row's [0, visible) alone; here the selection of a row starts in the scoring
- * kernel as soon as every tile of the row is stored, with the logits still in
- * L2, instead of after a second launch.
+ * row's [0, visible) alone.  The call runs the scoring launch and the top-k
+ * launch, which measure faster on GB300 than selecting inside the scoring
+ * kernel; with QSA_VARIANT_UMMA_TOPK forced (qsa_force_variant), a row's
+ * selection starts in the scoring kernel as soon as every tile of the row is
+ * stored, with the logits still in L2.
  *
  * Results: out_logits exactly as qsa_paged_mqa_logits_ex writes them; out_idx
  * exactly as qsa_select_topk(out_logits, R, out_cols, n, k, out_idx) writes
@@ -221,11 +223,11 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
  *   max_visible  host value: the caller's bound on the visible counts, or 0
  *                (unknown; out_cols and the page capacity bound them).  Like
  *                vLLM #62589's single_row_decode flag it only steers the
- *                dispatch: the selection runs in the scoring kernel for at
- *                most 256 rows, one row a request, whose bound is at most
- *                16384 columns, and as a separate top-k launch (which splits
- *                long rows over a thread-block cluster) otherwise.  A wrong
- *                bound costs speed only.
+ *                dispatch of the forced fused kernel: the selection runs in
+ *                the scoring kernel for at most 256 rows whose bound is at
+ *                most 16384 columns, and as a separate top-k launch (which
+ *                splits long rows over a thread-block cluster) otherwise.  A
+ *                wrong bound costs speed only.
  *   out_idx      int32 [R][k] (device), 4-byte aligned.
  *   workspace    device memory of at least qsa_paged_mqa_topk_workspace(desc)
  *                bytes, 4-byte aligned (NULL when that size is 0).  It must
@@ -243,7 +245,7 @@ qsa_status qsa_paged_mqa_topk(const qsa_paged_desc* desc, int32_t q_dtype, const
                               size_t workspace_bytes, void* stream);
 
 /* Workspace bytes qsa_paged_mqa_topk needs for `desc` (host only; 0 when the
- * shape never runs the fused selection, e.g. several rows a request, unless
+ * call never selects inside the scoring kernel - every shape unless
  * QSA_VARIANT_UMMA_TOPK is forced): 4 * (2 * G + 1) for the G <= 256 row
  * groups of the tcgen05 scorer. */
 qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* bytes);
@@ -256,9 +258,10 @@ qsa_status qsa_paged_mqa_topk_workspace(const qsa_paged_desc* desc, size_t* byte
  * device array of 257 words, enough for 128 row groups.  A call that would
  * select inside the scoring kernel over more groups is rejected with
  * QSA_ERR_UNSUPPORTED before anything is enqueued; calls that take the
- * scoring and top-k launches instead (more than 256 rows, rows longer than
- * 16384 columns, the CUDA-core scorer's shapes) never touch the array and
- * take any number of groups.  The array must read zero when a call starts: it
+ * scoring and top-k launches instead (every call unless QSA_VARIANT_UMMA_TOPK
+ * is forced, and then more than 256 rows, rows longer than 16384 columns, the
+ * CUDA-core scorer's shapes) never touch the array and take any number of
+ * groups.  The array must read zero when a call starts: it
  * is zero when the library is loaded, and every call that completes leaves it
  * zero.  A call that set qsa_device_status bit 0 may not:
  * qsa_device_status(flags, 1) then zeroes the array as well as the fault word,
@@ -311,8 +314,7 @@ qsa_status qsa_plan_variant_ex(const qsa_paged_desc* desc, int32_t q_dtype, int3
  * the call return QSA_ERR_UNSUPPORTED, and qsa_paged_mqa_topk then runs it
  * and the top-k launch.  QSA_VARIANT_UMMA_TOPK makes qsa_paged_mqa_topk select
  * inside the scoring kernel for every shape the tcgen05 scorer serves (the
- * dispatch does so for single-row groups only) and leaves the scoring calls'
- * dispatch as it is.  Meant for tests and A/B measurements. */
+ * dispatch never does) and leaves the scoring calls' dispatch as it is.  Meant for tests and A/B measurements. */
 void qsa_force_variant(int32_t variant);
 
 /* Variant launched by this thread's last successful scoring call

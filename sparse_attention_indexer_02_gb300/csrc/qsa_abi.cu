@@ -255,16 +255,14 @@ constexpr int64_t kFuseMaxVisible = 16384;
 
 // Whether qsa_paged_mqa_topk may select inside the scoring kernel for `d`
 // (the row count and the caller's bound are checked at the call).  Measured on
-// GB300, the fused kernel is slower than the lean scorer and the top-k launch
-// for groups of several rows (tiny_mtp 12.1 vs 9.4 us), so the dispatch fuses
-// single-row groups only; QSA_VARIANT_UMMA_TOPK forced fuses every shape the
-// tcgen05 scorer serves, and any other forced variant none.
+// GB300, the lean scorer followed by the top-k launch is faster than the fused
+// kernel at every decode shape (single-row decode 17.9 vs 18.4 us a step,
+// tiny_mtp 9.1 vs 12.1 us), so the dispatch does not fuse; forcing
+// QSA_VARIANT_UMMA_TOPK fuses every shape the tcgen05 scorer serves.
 bool fusable(const qsa_paged_desc* d) {
   const char* why = nullptr;
   if (!qsa::umma_supports(*d, &why)) return false;
-  const int32_t forced = g_forced_variant.load();
-  if (forced == QSA_VARIANT_UMMA_TOPK) return true;
-  return forced == QSA_VARIANT_AUTO && d->rows_per_req == 1;
+  return g_forced_variant.load() == QSA_VARIANT_UMMA_TOPK;
 }
 
 // Workspace words of the fused selection for `d` (0: the shape is never fused).

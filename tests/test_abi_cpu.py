@@ -173,7 +173,9 @@ def test_dispatch_decisions(lib):
 
 
 def test_fused_call_workspace_size_and_argument_checks(lib):
-    """qsa_paged_mqa_topk: host checks before anything is enqueued."""
+    """qsa_paged_mqa_topk: host checks before anything is enqueued (the fused
+    kernel forced, so the call needs a workspace)."""
+    qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
     d = _desc(rows_per_req=1)  # 2 single-row requests: two row groups
     assert qsa.topk_workspace_bytes(d) == 4 * (2 * 2 + 1)
     # the CUDA-core scorer's shapes never run the fused selection
@@ -197,20 +199,22 @@ def test_fused_call_workspace_size_and_argument_checks(lib):
     assert e.value.status == qsa.QSA_ERR_UNSUPPORTED
     qsa.paged_mqa_topk(_desc(num_requests=0), None, None, None, None, None, None, 8, None, None, None, 0,
                        stream=0)  # no rows: nothing to do
+    qsa.force_variant(qsa.VARIANT_AUTO)
 
 
-def test_one_call_fuses_single_row_groups_only(lib):
-    """The dispatch of qsa_paged_mqa_topk: the selection inside the scoring
-    kernel for single-row requests (a workspace is needed), the two launches
-    for several rows a request (measured faster; no workspace) unless
-    QSA_VARIANT_UMMA_TOPK is forced, and never for a forced scorer."""
+def test_one_call_fuses_only_when_forced(lib):
+    """The dispatch of qsa_paged_mqa_topk: the scoring and top-k launches
+    (measured faster than the fused kernel at every decode shape; no
+    workspace), the selection inside the scoring kernel only with
+    QSA_VARIANT_UMMA_TOPK forced (a workspace), never for a forced scorer."""
     qsa.force_variant(qsa.VARIANT_AUTO)
     try:
-        assert qsa.topk_workspace_bytes(_desc(rows_per_req=1)) == 4 * (2 * 2 + 1)
+        assert qsa.topk_workspace_bytes(_desc(rows_per_req=1)) == 0
         assert qsa.topk_workspace_bytes(_desc()) == 0
         assert qsa.topk_workspace_bytes(_desc(rows_per_req=1, page_cols=5, key_page_stride=5 * 256)) == 0
         qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
         assert qsa.topk_workspace_bytes(_desc()) == 4 * (2 * 2 + 1)
+        assert qsa.topk_workspace_bytes(_desc(rows_per_req=1)) == 4 * (2 * 2 + 1)
         assert qsa.plan_variant(_desc()) == qsa.VARIANT_UMMA_LEAN  # scoring dispatch unchanged
         for forced in (qsa.VARIANT_UMMA, qsa.VARIANT_UMMA_LEAN, qsa.VARIANT_ROWCORE):
             qsa.force_variant(forced)
@@ -220,12 +224,17 @@ def test_one_call_fuses_single_row_groups_only(lib):
 
 
 def test_noalloc_call_rejects_shapes_past_its_counters(lib):
-    """qsa_paged_mqa_topk_noalloc holds counters for 128 row groups: a larger
-    shape is refused before anything is enqueued."""
+    """qsa_paged_mqa_topk_noalloc holds counters for 128 row groups: a call
+    that would select inside the scoring kernel (forced) over more is refused
+    before anything is enqueued."""
     d = _desc(num_requests=200, rows_per_req=1)  # 200 groups of one row
-    with pytest.raises(qsa.QSAError) as e:
-        qsa._abi.paged_mqa_topk_noalloc(d, 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
-    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "128 row groups" in str(e.value)
-    with pytest.raises(qsa.QSAError) as e:  # the scoring checks come first
-        qsa._abi.paged_mqa_topk_noalloc(_desc(head_dim=64), 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
-    assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "head_dim" in str(e.value)
+    qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
+    try:
+        with pytest.raises(qsa.QSAError) as e:
+            qsa._abi.paged_mqa_topk_noalloc(d, 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
+        assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "128 row groups" in str(e.value)
+        with pytest.raises(qsa.QSAError) as e:  # the scoring checks come first
+            qsa._abi.paged_mqa_topk_noalloc(_desc(head_dim=64), 16, 16, 16, None, 16, 16, 8, 16, 16, stream=0)
+        assert e.value.status == qsa.QSA_ERR_UNSUPPORTED and "head_dim" in str(e.value)
+    finally:
+        qsa.force_variant(qsa.VARIANT_AUTO)
