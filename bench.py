@@ -9,8 +9,8 @@ call).  Prints one JSON line.
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 
 Timing: K steps back to back on one stream between a barrier and a device
-synchronize on both sides, enqueued as CUDA graph replays (>= 16 steps a
-graph) so host launch overhead is not on the device timeline; CUDA events
+synchronize on both sides, enqueued as CUDA graph replays (one graph of the K
+steps up to 256) so host launch overhead is not on the device timeline; CUDA events
 around the K steps give the step time, and graphs of scoring-only and
 top-k-only launches give each kernel's average launch time.  Inputs and
 outputs rotate over enough copies that their footprint exceeds twice the L2,
@@ -565,10 +565,11 @@ def run_gpu(args):
         W.one_call(d)
     torch.cuda.synchronize(dev)
 
-    # the timed region: K steps as graph replays (>= 16 steps a graph), so host
-    # launch overhead is not on the device timeline
+    # the timed region: K steps as graph replays - one graph of exactly K steps
+    # up to 256, else graphs of 256 and one of the rest - so host launch
+    # overhead is not on the device timeline
     K = args.steps
-    per_graph = W.per_graph
+    per_graph = K if K <= 256 else 256
     full_graphs, rem = divmod(K, per_graph)
     g_step = W.capture(per_graph, form)
     g_rem = W.capture(rem, form) if rem else None
