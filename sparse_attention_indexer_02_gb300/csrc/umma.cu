@@ -182,6 +182,7 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
   up.scales = p.scales;
   up.scale_stride = p.scale_page_stride;
   up.weights = p.weights;
+  up.q = p.q;
   up.block_table = p.block_table;
   up.visible = p.visible;
   up.next_n_lens = p.next_n_lens;

@@ -10,7 +10,8 @@
 // reduces heads in registers, and its stores of one row are 32 consecutive
 // floats per warp.
 //
-// Structure (one persistent CTA per SM, 16 warps; 14 with the converter):
+// Structure (one persistent CTA per SM, 16 warps; 15 in the converter form;
+// two CTAs of 8 warps per SM in the lean form):
 //  * schedule: every CTA derives, from the visible counts, the tile count of
 //    each row group (tiles past the group's widest visible column are never
 //    scheduled - the early exit of vLLM #62589 "Overview") and takes an equal
@@ -24,20 +25,25 @@
 //    copies into a 128-byte-swizzled stage (aiter #4221 KVBlockSize>=1 commit:
 //    block = table[b][col / page_cols], slot = col % page_cols).  A new group's
 //    q is loaded by a 2-D tensor copy once the previous group's MMAs are done.
-//  * warp 1 (MMA): one thread issues 8 tcgen05.mma (K = 16 each) per tile into
-//    one of two TMEM accumulators and commits the stage back to the producer.
+//  * warp 1 (MMA): the warp walks the tiles and an elected lane issues 8
+//    tcgen05.mma (K = 16 each; 4 of K = 32 with fp8 q) per tile into one of
+//    the TMEM accumulators, then commits the stage back to the producer.
 //  * warps 2-13 (epilogue, three warps per TMEM lane quadrant, each taking
-//    every third row block of the group; four warps with the converter):
-//    tcgen05.ld of the tile's columns, per head ReLU * weight, head sum,
-//    +0.0, -inf past the row's visible count, store.
-//  * warps 14-15 (bf16 keys or fp8 q): the -inf tail; with fp8 keys and bf16
-//    q, warps 6-13 instead widen each e4m3 key tile to bf16 for the MMA.
+//    every third row block of the group): tcgen05.ld of the tile's columns,
+//    per head ReLU * weight, head sum, +0.0, -inf past the row's visible
+//    count, store.  Warps 14-15 write the -inf tail.
+//  * converter form (fp8 keys, bf16 q): warps 2-9 are the epilogue in two sets
+//    of four taking alternate tiles; warps 10-13 widen each e4m3 key row to
+//    f16 (into TMEM, the MMA's A operand, or shared memory for N > 128) and
+//    scale each group's q into f16; warp 14 is a second MMA warp, the two
+//    taking alternate tiles.
 //  * FUSE instantiations (qsa_paged_mqa_topk) then select the rows of the row
 //    groups whose last tile this CTA stored (see "fused selection" below).
 // Every barrier wait gives up after about a second, sets the device fault
 // word (qsa_device_status) and lets the CTA drain and exit.
 #pragma once
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "device_common.cuh"
 #include "qsa_internal.h"
@@ -48,7 +54,7 @@ namespace qsa {
 namespace umma {
 
 constexpr int kKindBf16 = 0;                // bf16 keys, bf16 q
-constexpr int kKindFp8Keys = 1;             // fp8 keys widened to bf16 in shared memory, bf16 q
+constexpr int kKindFp8Keys = 1;             // fp8 keys widened to f16 by converter warps, bf16 q scaled to f16
 constexpr int kKindFp8Q = 2;                // fp8 keys, fp8 q: kind::f8f6f4 MMA
 constexpr int kBM = 128;                    // keys per tile (MMA M)
 constexpr int kHalfBytes = kBM * 128;       // one 64-element K-half of a bf16 key tile
@@ -59,15 +65,16 @@ constexpr int kTileBytes = 2 * kHalfBytes;  // 32 KB
 // K-half h of 8-key group i at h * 1024 + i * 2048.
 constexpr uint32_t kBf16AtomStride = 2048;
 constexpr int kFp8StageBytes = kBM * 128;  // 128 fp8 keys of 128 bytes
-constexpr int kFp8ConvStages = 3;          // bf16 operand stages fed by the converter
+constexpr int kFp8ConvStages = 3;          // f16 operand stages in shared memory fed by the converter
+constexpr int kFp8TmemStages = 4;          // ... or in TMEM (64 columns each)
 constexpr int kFp8StageAlloc = kFp8StageBytes + 1024;  // + the block's 128 fp32 scales, 1024-aligned
-constexpr int kScaleRing = kFp8ConvStages + 2;        // per-tile scale slots (see the converter)
+constexpr int kScaleRing = 8;                          // per-tile scale slots (see the converter)
 // fp8 q: the copies put each tile's key scales in their own slot of a ring (a
 // slot per tile, reused kQ8Ring tiles later), so a key stage is free as soon
 // as the MMA has read it; at most kQ8Ring - 2 key stages (see the producer).
 constexpr int kQ8Ring = 10;
 // Warp roles: 0 TMA, 1 MMA, then the epilogue warps (three per TMEM lane
-// quadrant, or one with the fp8 -> bf16 converter or in the lean form), then
+// quadrant, or one with the fp8 -> f16 converter or in the lean form), then
 // 8 converter warps (fp8 keys with bf16 q) or 2 spare warps that write the
 // -inf tail (ptxas 13.0 for aarch64 hosts crashes on this kernel when no warps
 // follow the epilogue).  The lean form (8 warps, at most 128 registers a
@@ -77,11 +84,18 @@ constexpr int kQ8Ring = 10;
 // still runs, and stream keys the moment it completes.
 template <bool CONV, bool LEAN = false>
 struct Roles {
-  static constexpr int kEpiWarps = (CONV || LEAN) ? 4 : 12;
+  static constexpr int kEpiWarps = CONV ? 8 : (LEAN ? 4 : 12);
   static constexpr int kEpiThreads = 32 * kEpiWarps;
-  static constexpr int kConvWarps = CONV ? 8 : 2;
+  static constexpr int kConvWarps = CONV ? 4 : 2;
+  // epilogue sets taking alternate tiles (the converter form's 64-head
+  // epilogue at one warp a lane quadrant would pace its pipeline)
+  static constexpr int kSets = CONV ? 2 : 1;
   static constexpr int kConvThreads = 32 * kConvWarps;
-  static constexpr int kThreads = 64 + kEpiThreads + kConvThreads;
+  // MMA warps: the converter form has a second one (the last warp), the two
+  // taking alternate tiles so that one's barrier waits overlap the other's
+  // MMAs (a tile there is only 8 x 32 cycles of tensor work)
+  static constexpr int kMmaWarps = CONV ? 2 : 1;
+  static constexpr int kThreads = 64 + kEpiThreads + kConvThreads + 32 * (kMmaWarps - 1);
 };
 constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kFastSchedRows = 256;              // up to this many rows one warp builds the schedule
@@ -102,6 +116,7 @@ struct UmmaParams {
   const uint8_t* scales;  // fp8: scale of (page, slot) at scales + page * scale_stride + 4 * slot
   int64_t scale_stride;
   const float* weights;
+  const uint16_t* q;  // bf16 q, [row x head][128] (the converter form reads it for its scales)
   const int32_t* block_table;
   const int32_t* visible;
   const int32_t* next_n_lens;  // live rows per request, or null (all live)
@@ -126,8 +141,11 @@ struct Layout {
   int32_t n;            // MMA N (rows x heads of a group, padded to 16..256)
   int32_t stages;       // TMA stages in flight (bf16 key tiles, or fp8 key tiles)
   int32_t stage_bytes;  // 32 KB (bf16 tile) or 16 KB (fp8 tile)
-  int32_t a_stages;     // fp8: bf16 operand stages written by the converter; bf16: 0
-  int32_t tmem_cols;    // 2 accumulators of N columns, power of two >= 32
+  int32_t a_stages;     // fp8: f16 operand stages written by the converter; bf16: 0
+  int32_t a_tmem;       // fp8 with N <= 128: the widened keys (MMA operand A) in TMEM, not smem
+  int32_t naccs;        // TMEM accumulators of N columns: 4 (converter form, N <= 64) or 2
+  int32_t a_col;        // a_tmem: TMEM column of the first A stage (after the accumulators)
+  int32_t tmem_cols;    // naccs x N (+ the A stages) columns, power of two >= 32
   uint32_t idesc;       // tcgen05 instruction descriptor for M = 128, this N
   int32_t a_off, b_off, ring_off, bar_off, misc_off, epi_off, sched_off, fuse_off, total;
 };
@@ -136,24 +154,32 @@ inline Layout make_layout(int N, int groups, int kind, bool fused = false, bool 
   const bool conv = kind == kKindFp8Keys, q8 = kind == kKindFp8Q;
   Layout L;
   L.n = N;
-  L.tmem_cols = 32;  // two accumulators of N columns, allocated as a power of two
-  while (L.tmem_cols < 2 * N) L.tmem_cols *= 2;
-  L.idesc = q8 ? ptx::idesc_e4m3_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N);
+  // fp8 keys widened by the converter: into TMEM beside the accumulators
+  // while they fit there (N <= 128), sparing shared memory 64 KB of traffic
+  // a tile (the widened keys' stores and the MMA's reads of them)
+  L.a_tmem = conv && N <= 128 ? 1 : 0;
+  L.naccs = L.a_tmem && N <= 64 ? 4 : 2;
+  L.a_col = L.naccs * N;
+  L.tmem_cols = 32;  // allocated as a power of two
+  while (L.tmem_cols < L.a_col + (L.a_tmem ? kFp8TmemStages * 64 : 0)) L.tmem_cols *= 2;
+  // the converter form computes in f16 (widened keys, q scaled into f16)
+  L.idesc = q8 ? ptx::idesc_e4m3_f32(kBM, N) : (conv ? ptx::idesc_f16_f32(kBM, N) : ptx::idesc_bf16_f32(kBM, N));
   // fp8 keys widened by the converter: the tile's scales ride in its stage
   L.stage_bytes = conv ? kFp8StageAlloc : (q8 ? kFp8StageBytes : kTileBytes);
-  L.a_stages = conv ? kFp8ConvStages : 0;
+  L.a_stages = conv ? (L.a_tmem ? kFp8TmemStages : kFp8ConvStages) : 0;
+  const int a_bytes = L.a_tmem ? 0 : L.a_stages * kTileBytes;  // smem for the widened keys
   const int qbytes = N * (q8 ? 128 : 256);         // q: N rows of D elements
   const int nring = conv ? kScaleRing : (q8 ? kQ8Ring : 0);
   const int ring = nring * kBM * 4;
-  const int tail = qbytes + ring + (2 * 8 + 2 * kFp8ConvStages + nring + 8) * 8 + 32 + 2 * 256 * 4 + 16 +
+  const int tail = qbytes + ring + (2 * 8 + 2 * kFp8TmemStages + nring + 13) * 8 + 32 + 2 * 256 * 4 + 16 +
                    8 * (groups + 1) + (fused ? 16 + 4 * kFuseWords : 0);
-  int st = ((lean ? kLeanSmem : kMaxSmem) - 1024 - tail - L.a_stages * kTileBytes) / L.stage_bytes;
+  int st = ((lean ? kLeanSmem : kMaxSmem) - 1024 - tail - a_bytes) / L.stage_bytes;
   L.stages = st > 8 ? 8 : st;  // <= kQ8Ring - 2
   L.a_off = L.stages * L.stage_bytes;  // fp8 only: the converter's bf16 ring
-  L.b_off = L.a_off + L.a_stages * kTileBytes;
+  L.b_off = L.a_off + a_bytes;
   L.ring_off = L.b_off + qbytes;       // fp8 only: per-tile key scales
   L.bar_off = L.ring_off + ring;
-  const int nbars = 2 * L.stages + 2 * L.a_stages + nring + 2 + 2 + 4;
+  const int nbars = 2 * L.stages + 2 * L.a_stages + nring + 4 + 4 + 5;
   L.misc_off = L.bar_off + nbars * 8;           // tmem slot, abort flag
   L.epi_off = (L.misc_off + 16 + 15) & ~15;     // w_s[256], vis_s[256]
   L.sched_off = L.epi_off + 2 * 256 * 4 + 16;   // pref[G + 1], gmax[G]
@@ -215,19 +241,66 @@ __device__ __forceinline__ void epi_bar(int nthreads) {
   asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Two fp8 e4m3 codes (bytes 0 and 1, or 2 and 3, of w) -> bf16x2, exactly.
-// The code's 7 magnitude bits placed at bf16 bits 10..4 give a bf16 with
-// exponent field eeee and fraction mmm0000, i.e. 2^(e-127) * 1.mmm (or the
-// subnormal 2^-126 * 0.mmm); one exact multiply by 2^120 rebiases it to the
-// e4m3 value 2^(e-7) * 1.mmm (or 2^-6 * 0.mmm).  The NaN codes S.1111.111 are
-// not inputs of this path.
+// Two fp8 e4m3 codes (bytes 0 and 1, or 2 and 3, of w) -> f16x2, the lower
+// code in the low half: the hardware conversion, exact (every e4m3 value,
+// 2^-9 .. 448, is an f16).  The NaN codes S.1111.111 are not inputs of this
+// path.
 template <int HI>
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t w) {
-  const uint32_t t = __byte_perm(w, 0u, HI ? 0x4342u : 0x4140u);  // code0 -> bits 0..7, code1 -> bits 16..23
-  const uint32_t bits = ((t & 0x00800080u) << 8) | ((t & 0x007F007Fu) << 4);
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  const uint16_t codes = (uint16_t)(HI ? (w >> 16) : (w & 0xFFFFu));
   uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(bits), "r"(0x7B807B80u));  // 2^120 in both halves
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(codes));
   return r;
+}
+
+// The converter form runs its MMA in f16 (the widened fp8 keys are exact
+// there).  A q row-head (128 bf16 elements) enters as q * 2^-e, with e taken
+// from its largest magnitude so that this lies in [2^14, 2^15): every bf16
+// element at or above 2^-17 there (8 significant bits on f16's grid of
+// 2^-24 and finer) is then an f16 exactly, and smaller ones, under 2^-31 of
+// the largest, round at 2^-25.  The head's weight is multiplied by 2^e.
+// Products with powers of two commute with fp32 rounding, so each head's
+// term w * relu(s x) is the one the bf16 MMA gives, bit for bit, while 2^e w
+// stays a normal fp32 number.  Rows of zeros, or with an infinity or NaN,
+// take e = 0.
+//
+// e from the bit pattern of the largest magnitude (sign cleared), by integer
+// arithmetic alone, so the converter (from its shared-memory copy of q) and
+// the epilogue (from q in global memory) reach the same value.
+__device__ __forceinline__ int q_row_exp(uint32_t amax_bits) {
+  const uint32_t ex = amax_bits >> 7, mant = amax_bits & 0x7Fu;
+  if (amax_bits == 0 || ex == 0xFFu) return 0;
+  const int lg = ex != 0 ? (int)ex - 127 : (31 - __clz((int)mant)) - 133;  // floor(log2 |q|max)
+  return lg - 14;
+}
+
+// 2^e as fp32, exactly, for e in [-149, 127].
+__device__ __forceinline__ float pow2_exact(int e) {
+  return e >= -126 ? __int_as_float((e + 127) << 23) : __int_as_float(1 << (e + 149));
+}
+
+// Largest magnitude bit pattern of the 8 bf16 elements in v.
+__device__ __forceinline__ uint32_t bf16x8_amax_bits(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) m = max(m, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+  return m;
+}
+
+// The 8 bf16 elements of v times 2^s1 * 2^s2 (two exact steps: the scale
+// 2^-e itself may exceed fp32's range), rounded to f16.
+__device__ __forceinline__ uint4 bf16x8_scaled_to_f16(uint4 v, float s1, float s2) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16) * s1 * s2;
+    const float hi = __uint_as_float(w[i] & 0xFFFF0000u) * s1 * s2;
+    const __half2 h = __floats2half2_rn(lo, hi);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // The -inf tail: group g's columns [T_g * 128, out_cols) for its rows, where
@@ -409,7 +482,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     umma_score_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                       const UmmaParams p, const Layout L) {
   constexpr bool FP8 = KIND != kKindBf16;      // fp8 keys (+ per-key scales)
-  constexpr bool CONV = KIND == kKindFp8Keys;  // widened to bf16 by the converter warps
+  constexpr bool CONV = KIND == kKindFp8Keys;  // widened to f16 by the converter warps
   constexpr bool Q8 = KIND == kKindFp8Q;       // fp8 q: e4m3 x e4m3 MMA on the copied keys
   static_assert(!LEAN || (!CONV && !FUSE), "the lean form has no converter and no fused selection");
   using R = Roles<CONV, LEAN>;
@@ -432,8 +505,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
   uint64_t* sfull = aempty + kAStages;        // fp8: scales of a tile ready, one per scale slot
   uint64_t* tfull = sfull + (CONV ? kScaleRing : (Q8 ? kQ8Ring : 0));
   float* scale_ring = reinterpret_cast<float*>(smem + L.ring_off);  // fp8: [slots][128]
-  uint64_t* tempty = tfull + 2;
-  uint64_t* qfull = tempty + 2;
+  uint64_t* tempty = tfull + 4;
+  uint64_t* qfull = tempty + 4;
   uint64_t* qempty = qfull + 1;
   uint64_t* mma_done = qempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.misc_off);
@@ -449,6 +522,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
   const int G = p.num_groups;
 
   uint64_t* setup = mma_done + 1;  // one-warp schedule and TMEM allocation done
+  uint64_t* qready = setup + 1;    // converter form: the group's q scaled into f16 in place
   // Few rows: warp 0 alone builds the schedule from visible counts it loads
   // first thing, and starts producing at once; the other warps wait on
   // `setup`.  Many rows: every thread takes part, with CTA barriers.
@@ -457,24 +531,25 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       // freed by the converter (widened keys), or by the MMA
-      ptx::mbar_init(&empty[s], CONV ? R::kConvThreads : 1);
+      ptx::mbar_init(&empty[s], CONV ? R::kConvWarps : 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      ptx::mbar_init(&afull[s], R::kConvThreads);
+      ptx::mbar_init(&afull[s], R::kConvWarps);
       ptx::mbar_init(&aempty[s], 1);
     }
     if (CONV)
-      for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], kBM);
+      for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], R::kConvWarps);
     if (Q8)
       for (int s = 0; s < kQ8Ring; ++s) ptx::mbar_init(&sfull[s], 1);
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < L.naccs; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], kEpiThreads);
+      ptx::mbar_init(&tempty[a], R::kEpiWarps / R::kSets);  // a warp of the set that read it
     }
     ptx::mbar_init(qfull, 1);
-    ptx::mbar_init(qempty, 1);
-    ptx::mbar_init(mma_done, 1);
+    ptx::mbar_init(qempty, R::kMmaWarps);
+    ptx::mbar_init(mma_done, R::kMmaWarps);
     ptx::mbar_init(setup, 2);
+    ptx::mbar_init(qready, CONV ? R::kConvWarps : 1);
     *abort_flag = 0;
     if (FUSE) fz[0] = 0;
     ptx::fence_mbar_init();
@@ -734,79 +809,105 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
           }
         }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || (R::kMmaWarps > 1 && warp == 2 + R::kEpiWarps + R::kConvWarps)) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, acc_phase = 0;
-      int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
-      int qg = -1;
-      uint32_t q_uses = 0;
-      const uint32_t a_base = ptx::smem_u32(A);
-      const uint32_t b_base = ptx::smem_u32(Bq);
-      bool ok = true;
-      for (int t = t_begin; t < t_end && ok; ++t) {
-        while (t >= pref[g + 1]) ++g;
-        if (g != qg) {
-          if (qg >= 0) ptx::mma_commit(qempty);  // q buffer free once earlier MMAs finish
-          ok = wait_phase(qfull, q_uses & 1u, abort_flag, p.fault);
-          if (!ok) break;
-          ++q_uses;
-          qg = g;
-        }
-        ok = wait_phase(&tempty[acc], acc_phase ^ 1u, abort_flag, p.fault);
+    // The whole warp runs the loop and one elected lane issues each tcgen05
+    // instruction (the operands stay warp-uniform).  Waits are warp-wide: a
+    // lane's failed wait ends the loop for every lane.  With two MMA warps,
+    // warp mw issues the tiles with (t - t_begin) % 2 == mw; both follow the
+    // group changes (each releases the q buffer for its own MMAs).
+    const int mw = warp == 1 ? 0 : 1;
+    auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, p.fault));
+    };
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
+    int qg = -1;
+    uint32_t q_uses = 0;
+    const uint32_t a_base = ptx::smem_u32(A);
+    const uint32_t b_base = ptx::smem_u32(Bq);
+    bool ok = true;
+    for (int t = t_begin; t < t_end && ok; ++t) {
+      while (t >= pref[g + 1]) ++g;
+      if (g != qg) {
+        if (qg >= 0) ptx::mma_commit_elect(qempty);  // q buffer free once earlier MMAs finish
+        ok = warp_wait(CONV ? qready : qfull, q_uses & 1u);
         if (!ok) break;
-        ptx::tc_fence_after();
-        ok = wait_phase(CONV ? &afull[stage] : &full[stage], phase, abort_flag, p.fault);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * N);
-        if (Q8) {
-          // the fp8 key rows as copied: 128 bytes (all of D) a key, 4 MMAs of K = 32
-          const uint32_t a0 = a_base + stage * (uint32_t)L.stage_bytes;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = ptx::sw128_desc(a0 + (uint32_t)k * 32u);
-            const uint64_t bd = ptx::sw128_desc(b_base + (uint32_t)k * 32u);
-            ptx::mma_e4m3(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
-          }
-        } else {
-          const uint32_t a0 = a_base + stage * kTileBytes;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t koff = (uint32_t)(k & 3) * 32u;
-            // copied bf16 keys: halves interleaved per 8-key group; widened
-            // fp8 keys: one 16 KB block per K-half
-            const uint64_t ad = CONV ? ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff)
-                                     : ptx::sw128_desc(a0 + (k >> 2) * 1024u + koff, kBf16AtomStride);
-            const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
-            ptx::mma_bf16(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
-          }
-        }
-        ptx::mma_commit(CONV ? &aempty[stage] : &empty[stage]);
-        ptx::mma_commit(&tfull[acc]);
+        ++q_uses;
+        qg = g;
+      }
+      if (R::kMmaWarps > 1 && ((t - t_begin) & 1) != mw) {  // the other MMA warp's tile
         if (++stage == (CONV ? kAStages : kStages)) {
           stage = 0;
           phase ^= 1u;
         }
-        if (++acc == 2) {
+        if (++acc == L.naccs) {
           acc = 0;
           acc_phase ^= 1u;
         }
+        continue;
       }
-      // every MMA issued above has completed before TMEM is released
-      ptx::mma_commit(mma_done);
-      const long long t0 = clock64();
-      while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinCycles) {
+      ok = warp_wait(&tempty[acc], acc_phase ^ 1u) && warp_wait(CONV ? &afull[stage] : &full[stage], phase);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)(acc * N);
+      if (Q8) {
+        // the fp8 key rows as copied: 128 bytes (all of D) a key, 4 MMAs of K = 32
+        const uint32_t a0 = a_base + stage * (uint32_t)L.stage_bytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t ad = ptx::sw128_desc(a0 + (uint32_t)k * 32u);
+          const uint64_t bd = ptx::sw128_desc(b_base + (uint32_t)k * 32u);
+          ptx::mma_e4m3_elect(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+        }
+      } else if (CONV && L.a_tmem) {
+        // the widened keys in TMEM: K elements 16k .. 16k + 15 of every
+        // key row in columns 8k .. 8k + 7 of the stage
+        const uint32_t at = tmem_base + (uint32_t)(L.a_col + stage * 64);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + (uint32_t)(k & 3) * 32u);
+          ptx::mma_bf16_ts_elect(d, at + 8u * (uint32_t)k, bd, L.idesc, k > 0 ? 1u : 0u);
+        }
+      } else {
+        const uint32_t a0 = a_base + stage * kTileBytes;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t koff = (uint32_t)(k & 3) * 32u;
+          // copied bf16 keys: halves interleaved per 8-key group; widened
+          // fp8 keys in shared memory: one 16 KB block per K-half
+          const uint64_t ad = CONV ? ptx::sw128_desc(a0 + (k >> 2) * kHalfBytes + koff)
+                                   : ptx::sw128_desc(a0 + (k >> 2) * 1024u + koff, kBf16AtomStride);
+          const uint64_t bd = ptx::sw128_desc(b_base + (k >> 2) * (N * 128) + koff);
+          ptx::mma_bf16_elect(d, ad, bd, L.idesc, k > 0 ? 1u : 0u);
+        }
       }
+      ptx::mma_commit_elect(CONV ? &aempty[stage] : &empty[stage]);
+      ptx::mma_commit_elect(&tfull[acc]);
+      if (++stage == (CONV ? kAStages : kStages)) {
+        stage = 0;
+        phase ^= 1u;
+      }
+      if (++acc == L.naccs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    // every MMA issued above has completed before TMEM is released
+    ptx::mma_commit_elect(mma_done);
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(mma_done, 0) && clock64() - t0 < kSpinCycles) {
     }
     __syncwarp();
   } else if (warp < 2 + R::kEpiWarps) {
     // ------------------------------------------------------------ epilogue
-    constexpr int kHalves = R::kEpiWarps / 4;  // warps sharing one TMEM lane quadrant
-    const int et = threadIdx.x - 64;           // 0 .. kEpiThreads - 1
-    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int half = (warp - 2) >> 2;          // which of the quadrant's warps
+    constexpr int kSets = R::kSets;                      // sets taking alternate tiles
+    constexpr int kHalves = R::kEpiWarps / (4 * kSets);  // a set's warps sharing one TMEM lane quadrant
+    const int et = threadIdx.x - 64;                     // 0 .. kEpiThreads - 1
+    const int quad = warp & 3;                           // TMEM lane quadrant this warp may access
+    const int set = (warp - 2) / (4 * kHalves);          // this warp's set
+    const int half = ((warp - 2) >> 2) % kHalves;        // which of the set's quadrant warps
     const int m = quad * 32 + lane;            // key row of the tile = TMEM lane
     const int64_t oc = p.out_cols;
     const bool stream_out = p.stream_out != 0;
@@ -819,8 +920,9 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     constexpr int kRowsPerUnit = H >= 16 ? 1 : 16 / H;
     constexpr int kLdPerUnit = H >= 16 ? H / 16 : 1;
     constexpr int kUnitsPerBatch = 4 / kLdPerUnit;  // four loads in flight
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    // tile i of the CTA: set i % kSets, accumulator i % naccs, in its
+    // (i / naccs)-th use
+    const int lg_accs = L.naccs == 4 ? 2 : 1;
     int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
     int eg = -1, r0 = 0, nr = 0, b = 0;
     int run = 0;  // FUSE: tiles of group eg stored in this CTA's current run
@@ -838,7 +940,19 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         r0 = b * p.rows_per_req + jj * p.group_rows;
         nr = min(p.group_rows, p.rows_per_req - jj * p.group_rows);
         if (et == 0) *vis_min_s = INT32_MAX;
-        for (int i = et; i < nr * H; i += kEpiThreads) w_s[i] = p.weights[(int64_t)r0 * H + i];
+        for (int i = et; i < nr * H; i += kEpiThreads) {
+          float w = p.weights[(int64_t)r0 * H + i];
+          if (CONV) {
+            // the row-head's q enters the f16 MMA as q * 2^-e: its weight
+            // takes 2^e (e from q in global memory, as the converter found it)
+            const uint4* qr = reinterpret_cast<const uint4*>(p.q + ((int64_t)r0 * H + i) * 128);
+            uint32_t amax = 0;
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) amax = max(amax, bf16x8_amax_bits(__ldg(qr + j)));
+            w *= pow2_exact(q_row_exp(amax));
+          }
+          w_s[i] = w;
+        }
         epi_bar(kEpiThreads);
         for (int i = et; i < nr; i += kEpiThreads) {
           const int32_t v = (int32_t)row_visible(p.visible, p.next_n_lens, r0 + i, p.rows_per_req, p.capacity);
@@ -850,6 +964,10 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
       }
       ++run;
       if (!ok) continue;
+      const int ti = t - t_begin;
+      if (kSets > 1 && ti % kSets != set) continue;  // the other set's tile
+      const int acc = ti & (L.naccs - 1);
+      const uint32_t acc_phase = (uint32_t)(ti >> lg_accs) & 1u;
       const int tile_c0 = (t - pref[g]) * kBM;  // first column of the tile
       const int64_t c = (int64_t)tile_c0 + m;
       // every row of the group sees the whole tile: no mask, no bounds test
@@ -859,23 +977,25 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
       // per row after the head sum.
       float sgn = 1.0f, mag = 1.0f;
       if (CONV) {
-        const int i = t - t_begin;
-        ok = wait_phase(&sfull[i % kScaleRing], (uint32_t)(i / kScaleRing) & 1u, abort_flag, p.fault);
+        ok = __all_sync(0xffffffffu,
+                        wait_phase(&sfull[ti % kScaleRing], (uint32_t)(ti / kScaleRing) & 1u, abort_flag, p.fault));
         if (!ok) continue;
-        const float sc = scale_ring[(i % kScaleRing) * kBM + m];
+        const float sc = scale_ring[(ti % kScaleRing) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       } else if (Q8) {
         // the tile's scales, copied into their slot of the scale ring;
         // waiting on the slot's completed fill orders the copied bytes
-        const int i = t - t_begin;
-        ok = wait_phase(&sfull[i % kQ8Ring], (uint32_t)(i / kQ8Ring) & 1u, abort_flag, p.fault);
+        ok = __all_sync(0xffffffffu,
+                        wait_phase(&sfull[ti % kQ8Ring], (uint32_t)(ti / kQ8Ring) & 1u, abort_flag, p.fault));
         if (!ok) continue;
-        const float sc = scale_ring[(i % kQ8Ring) * kBM + m];
+        const float sc = scale_ring[(ti % kQ8Ring) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
-      ok = wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault);
+      // waits are warp-wide (a lane's failure stops its whole warp): the TMEM
+      // loads below and the warp's single release need the warp together
+      ok = __all_sync(0xffffffffu, wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault));
       if (!ok) continue;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
@@ -986,12 +1106,11 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
           }
         }
       }
+      // every lane's loads are done (tcgen05.wait::ld above) and fenced;
+      // one arrival a warp releases the accumulator
       ptx::tc_fence_before();
-      ptx::mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
     }
     if (FUSE && eg >= 0) fuse_close(p, pref, eg, run, et, fz, kEpiThreads);
 
@@ -999,55 +1118,130 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     // converter warps are busy until then).  bf16: the spare warps write it.
     if (CONV && ok && setup_ok) fill_tail<kEpiThreads>(p, pref, G, total, et);
   } else if (CONV) {
-    // ------------------------------------------------------------ fp8 -> bf16 converter
-    // Thread (m, kh) widens the kh-th 64-element half of key row m.  The TMA
-    // stage holds 128-byte fp8 rows in the 128-byte swizzle (16-byte chunk j
-    // of row r at chunk j ^ (r % 8)); the bf16 operand rows use the same
-    // pattern, so both sides are bank-conflict free.
-    const int ct = threadIdx.x - 64 - kEpiThreads;  // 0..255
-    const int m = ct & (kBM - 1), kh = ct >> 7;
+    // ------------------------------------------------------------ fp8 -> f16 converter
+    // Thread m widens key row m.  The TMA stage holds 128-byte fp8 rows in
+    // the 128-byte swizzle (16-byte chunk j of row r at chunk j ^ (r % 8)).
+    // The widened row goes to TMEM lane m (row m of the MMA's A operand, two
+    // K elements a column), or, for N > 128, to the two K-half blocks of a
+    // shared-memory operand stage in the same swizzle (bank-conflict free on
+    // both sides).  Row m is in this warp's TMEM lane quadrant.
+    static_assert(!CONV || R::kConvThreads == kBM, "one converter thread a key row");
+    const int m = (warp & 3) * 32 + lane;
     const int sw = m & 7;
+    const bool a_tmem = L.a_tmem != 0;
+    const uint32_t a_lane = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)L.a_col;
+    const int cw = warp - (2 + R::kEpiWarps);  // converter warp 0..3
     int stage = 0, a = 0;
     uint32_t phase = 0, aphase = 0;
+    int g = t_begin < t_end ? find_group(pref, G, t_begin) : 0;
+    int qg = -1;
+    uint32_t q_uses = 0;
     bool ok = true;
     for (int t = t_begin; t < t_end && ok; ++t) {
-      ok = wait_phase(&full[stage], phase, abort_flag, p.fault);
-      if (!ok) break;
-      ok = wait_phase(&aempty[a], aphase ^ 1u, abort_flag, p.fault);
-      if (!ok) break;
-      const uint8_t* src = S + stage * L.stage_bytes + m * 128;
-      uint4 in[4];
+      while (t >= pref[g + 1]) ++g;
+      if (g != qg) {
+        // a new group's q (bf16, landed by the producer once the MMAs of the
+        // last group were done): scaled into f16 in place, each row-head by
+        // its 2^-e.  Half-warp h of this warp takes row-head n = 2 (cw + 4 i)
+        // + h; lane l of it the 16 bytes at chunk l % 8 of K-half l / 8 (the
+        // swizzle only permutes a row's chunks, and the conversion is per
+        // element).
+        ok = __all_sync(0xffffffffu, wait_phase(qfull, q_uses & 1u, abort_flag, p.fault));
+        if (!ok) break;
+        const int l16 = lane & 15;
+        for (int n0 = 2 * cw; n0 < N; n0 += 2 * R::kConvWarps) {
+          const int n = n0 + (lane >> 4);
+          uint4* qp = reinterpret_cast<uint4*>(Bq + (l16 >> 3) * (N * 128) + n * 128 + (l16 & 7) * 16);
+          const uint4 v = *qp;
+          uint32_t amax = bf16x8_amax_bits(v);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) in[i] = *reinterpret_cast<const uint4*>(src + (((4 * kh + i) ^ sw) << 4));
-      if (kh == 0) {
-        // Tile i's scales go to ring slot i % kScaleRing.  The slot is free:
-        // this converter may be at tile i only after the MMA of tile
-        // i - kScaleRing + kFp8ConvStages finished, which needed the epilogue
-        // to release the accumulator of tile i - kScaleRing (same parity), and
-        // the epilogue reads a tile's scales before releasing it.
+          for (int o = 8; o >= 1; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+          const int ne = -q_row_exp(amax);
+          *qp = bf16x8_scaled_to_f16(v, pow2_exact(ne / 2), pow2_exact(ne - ne / 2));
+        }
+        ptx::fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(qready);
+        ++q_uses;
+        qg = g;
+      }
+      ok = wait_phase(&full[stage], phase, abort_flag, p.fault) &&
+           wait_phase(&aempty[a], aphase ^ 1u, abort_flag, p.fault);
+      // the warp goes on together (the TMEM stores below are warp-wide)
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      ptx::tc_fence_after();  // after the MMA's reads of the stage's last use
+      const uint8_t* src = S + stage * L.stage_bytes + m * 128;
+      uint4 in[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) in[i] = *reinterpret_cast<const uint4*>(src + ((i ^ sw) << 4));
+      {
+        // Tile i's scales go to ring slot i % kScaleRing, last used by tile
+        // i - kScaleRing (kScaleRing even: same epilogue set as tile i).  It
+        // is free: before this point the converter waited, for tiles j = i - 1
+        // and i, until the MMA of tile j - a_stages had completed, and that
+        // MMA had waited for the epilogue to release accumulator use
+        // j - a_stages - naccs.  One of those two uses has the parity of i and
+        // is not before i - kScaleRing; its set works through its tiles in
+        // order and reads a tile's scales before releasing it.
+        static_assert(kScaleRing % 2 == 0 && kScaleRing >= kFp8TmemStages + 4 &&
+                          kScaleRing >= kFp8ConvStages + 2 + 1,
+                      "scale slot reuse");
         const int i = t - t_begin;
         scale_ring[(i % kScaleRing) * kBM + m] =
             *reinterpret_cast<const float*>(S + stage * L.stage_bytes + kFp8StageBytes + m * 4);
-        ptx::mbar_arrive(&sfull[i % kScaleRing]);
+        // one arrival a warp: its lanes' scale stores are out and their
+        // reads of the stage done
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(&sfull[i % kScaleRing]);
+          ptx::mbar_arrive(&empty[stage]);
+        }
       }
-      ptx::mbar_arrive(&empty[stage]);  // this thread's reads of the stage are done
-      uint8_t* dst = A + a * kTileBytes + kh * kHalfBytes + m * 128;
+      if (a_tmem) {
+        // columns 8j .. 8j + 7 of the stage: the 16 elements of fp8 chunk j,
+        // two to a column, the lower K index in the low half
+        const uint32_t ta = a_lane + (uint32_t)(a * 64);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint4 o0, o1;
-        o0.x = e4m3x2_to_bf16x2<0>(in[i].x);
-        o0.y = e4m3x2_to_bf16x2<1>(in[i].x);
-        o0.z = e4m3x2_to_bf16x2<0>(in[i].y);
-        o0.w = e4m3x2_to_bf16x2<1>(in[i].y);
-        o1.x = e4m3x2_to_bf16x2<0>(in[i].z);
-        o1.y = e4m3x2_to_bf16x2<1>(in[i].z);
-        o1.z = e4m3x2_to_bf16x2<0>(in[i].w);
-        o1.w = e4m3x2_to_bf16x2<1>(in[i].w);
-        *reinterpret_cast<uint4*>(dst + (((2 * i) ^ sw) << 4)) = o0;
-        *reinterpret_cast<uint4*>(dst + (((2 * i + 1) ^ sw) << 4)) = o1;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[16];
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint4 w = in[2 * c + jj];
+            o[8 * jj + 0] = e4m3x2_to_f16x2<0>(w.x);
+            o[8 * jj + 1] = e4m3x2_to_f16x2<1>(w.x);
+            o[8 * jj + 2] = e4m3x2_to_f16x2<0>(w.y);
+            o[8 * jj + 3] = e4m3x2_to_f16x2<1>(w.y);
+            o[8 * jj + 4] = e4m3x2_to_f16x2<0>(w.z);
+            o[8 * jj + 5] = e4m3x2_to_f16x2<1>(w.z);
+            o[8 * jj + 6] = e4m3x2_to_f16x2<0>(w.w);
+            o[8 * jj + 7] = e4m3x2_to_f16x2<1>(w.w);
+          }
+          ptx::tmem_st16(ta + 16u * (uint32_t)c, o);
+        }
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();  // the stores -> the MMA, through the barrier
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uint8_t* dst = A + a * kTileBytes + (i >> 2) * kHalfBytes + m * 128;
+          const int j = i & 3;  // 16-byte fp8 chunk j of the half: bf16 chunks 2j, 2j + 1
+          uint4 o0, o1;
+          o0.x = e4m3x2_to_f16x2<0>(in[i].x);
+          o0.y = e4m3x2_to_f16x2<1>(in[i].x);
+          o0.z = e4m3x2_to_f16x2<0>(in[i].y);
+          o0.w = e4m3x2_to_f16x2<1>(in[i].y);
+          o1.x = e4m3x2_to_f16x2<0>(in[i].z);
+          o1.y = e4m3x2_to_f16x2<1>(in[i].z);
+          o1.z = e4m3x2_to_f16x2<0>(in[i].w);
+          o1.w = e4m3x2_to_f16x2<1>(in[i].w);
+          *reinterpret_cast<uint4*>(dst + (((2 * j) ^ sw) << 4)) = o0;
+          *reinterpret_cast<uint4*>(dst + (((2 * j + 1) ^ sw) << 4)) = o1;
+        }
+        ptx::fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
       }
-      ptx::fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
-      ptx::mbar_arrive(&afull[a]);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&afull[a]);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
