@@ -531,19 +531,21 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full[s], 1);
       // freed by the converter (widened keys), or by the MMA
-      ptx::mbar_init(&empty[s], CONV ? R::kConvWarps : 1);
+      ptx::mbar_init(&empty[s], CONV ? R::kConvThreads : 1);
     }
     for (int s = 0; s < kAStages; ++s) {
-      ptx::mbar_init(&afull[s], R::kConvWarps);
+      ptx::mbar_init(&afull[s], R::kConvThreads);
       ptx::mbar_init(&aempty[s], 1);
     }
     if (CONV)
-      for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], R::kConvWarps);
+      for (int s = 0; s < kScaleRing; ++s) ptx::mbar_init(&sfull[s], R::kConvThreads);
     if (Q8)
       for (int s = 0; s < kQ8Ring; ++s) ptx::mbar_init(&sfull[s], 1);
     for (int a = 0; a < L.naccs; ++a) {
       ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], R::kEpiWarps / R::kSets);  // a warp of the set that read it
+      // released by each thread of the set that read it (one arrival a warp
+      // after __syncwarp measured slower: 422 against 413 us prefill scoring)
+      ptx::mbar_init(&tempty[a], kEpiThreads / R::kSets);
     }
     ptx::mbar_init(qfull, 1);
     ptx::mbar_init(qempty, R::kMmaWarps);
@@ -977,8 +979,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
       // per row after the head sum.
       float sgn = 1.0f, mag = 1.0f;
       if (CONV) {
-        ok = __all_sync(0xffffffffu,
-                        wait_phase(&sfull[ti % kScaleRing], (uint32_t)(ti / kScaleRing) & 1u, abort_flag, p.fault));
+        ok = wait_phase(&sfull[ti % kScaleRing], (uint32_t)(ti / kScaleRing) & 1u, abort_flag, p.fault);
         if (!ok) continue;
         const float sc = scale_ring[(ti % kScaleRing) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
@@ -986,16 +987,13 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
       } else if (Q8) {
         // the tile's scales, copied into their slot of the scale ring;
         // waiting on the slot's completed fill orders the copied bytes
-        ok = __all_sync(0xffffffffu,
-                        wait_phase(&sfull[ti % kQ8Ring], (uint32_t)(ti / kQ8Ring) & 1u, abort_flag, p.fault));
+        ok = wait_phase(&sfull[ti % kQ8Ring], (uint32_t)(ti / kQ8Ring) & 1u, abort_flag, p.fault);
         if (!ok) continue;
         const float sc = scale_ring[(ti % kQ8Ring) * kBM + m];
         sgn = sc < 0.0f ? -1.0f : 1.0f;
         mag = fabsf(sc);
       }
-      // waits are warp-wide (a lane's failure stops its whole warp): the TMEM
-      // loads below and the warp's single release need the warp together
-      ok = __all_sync(0xffffffffu, wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault));
+      ok = wait_phase(&tfull[acc], acc_phase, abort_flag, p.fault);
       if (!ok) continue;
       ptx::tc_fence_after();
       const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * N);
@@ -1106,11 +1104,9 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
           }
         }
       }
-      // every lane's loads are done (tcgen05.wait::ld above) and fenced;
-      // one arrival a warp releases the accumulator
+      // this thread's loads are done (tcgen05.wait::ld above) and fenced
       ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+      ptx::mbar_arrive(&tempty[acc]);
     }
     if (FUSE && eg >= 0) fuse_close(p, pref, eg, run, et, fz, kEpiThreads);
 
@@ -1190,13 +1186,8 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         const int i = t - t_begin;
         scale_ring[(i % kScaleRing) * kBM + m] =
             *reinterpret_cast<const float*>(S + stage * L.stage_bytes + kFp8StageBytes + m * 4);
-        // one arrival a warp: its lanes' scale stores are out and their
-        // reads of the stage done
-        __syncwarp();
-        if (lane == 0) {
-          ptx::mbar_arrive(&sfull[i % kScaleRing]);
-          ptx::mbar_arrive(&empty[stage]);
-        }
+        ptx::mbar_arrive(&sfull[i % kScaleRing]);
+        ptx::mbar_arrive(&empty[stage]);  // this thread's reads of the stage are done
       }
       if (a_tmem) {
         // columns 8j .. 8j + 7 of the stage: the 16 elements of fp8 chunk j,
@@ -1240,8 +1231,7 @@ __global__ void __launch_bounds__(Roles<KIND == kKindFp8Keys, LEAN>::kThreads, L
         }
         ptx::fence_proxy_async_smem();  // generic-proxy writes -> visible to tcgen05.mma
       }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&afull[a]);
+      ptx::mbar_arrive(&afull[a]);
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
