@@ -156,13 +156,14 @@ def source_sha(paths):
     return h.hexdigest()[:16]
 
 
+_CS = "sparse_attention_indexer_02_gb300/csrc/"
+_COMMON = [_CS + "device_common.cuh", _CS + "sm100_ptx.cuh"]  # headers every kernel below includes
 KERNEL_SOURCES = {
-    "rowcore": ["sparse_attention_indexer_02_gb300/csrc/rowcore.cu"],
-    "umma_lean": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
-    "umma": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu"],
-    "topk": ["sparse_attention_indexer_02_gb300/csrc/topk.cu", "sparse_attention_indexer_02_gb300/csrc/topk_select.cuh"],
-    "umma+topk": ["sparse_attention_indexer_02_gb300/csrc/umma_kernel.cuh", "sparse_attention_indexer_02_gb300/csrc/umma.cu",
-                  "sparse_attention_indexer_02_gb300/csrc/topk_select.cuh"],
+    "rowcore": [_CS + "rowcore.cu", _CS + "device_common.cuh"],
+    "umma_lean": [_CS + "umma_kernel.cuh", _CS + "umma.cu", _CS + "topk_select.cuh"] + _COMMON,
+    "umma": [_CS + "umma_kernel.cuh", _CS + "umma.cu", _CS + "topk_select.cuh"] + _COMMON,
+    "topk": [_CS + "topk.cu", _CS + "topk_select.cuh"] + _COMMON,
+    "umma+topk": [_CS + "umma_kernel.cuh", _CS + "umma.cu", _CS + "topk_select.cuh"] + _COMMON,
 }
 
 
@@ -412,6 +413,16 @@ class Workload:
                         if per_copy > 2 * l2 else f"single copy ({per_copy / 1e6:.0f} MB), L2 not defeated")
         self.max_visible = int(spec.live_visible().max()) if R else 0
         self.api = torch_api
+        # the pages the scorer reads (each request's pages holding a visible
+        # column of a live row), for the page-stream reference
+        need = spec.pages_needed()
+        self.page_list = np.concatenate([inp.block_table[b, :need[b]] for b in range(spec.num_requests)]
+                                        ).astype(np.int32) if spec.num_requests else np.zeros(0, np.int32)
+        self.page_bytes = inp.key_page_stride  # a whole page: bf16 keys, or fp8 keys and their scales
+        pages_dev = torch.from_numpy(self.page_list).to(dev)
+        for d in self.sets:
+            d["pages"] = pages_dev
+            d["pcheck"] = torch.zeros(1, dtype=torch.int32, device=dev)
         self.per_graph = copies * max(1, -(-16 // copies))
 
     def score(self, d):
@@ -419,6 +430,10 @@ class Workload:
         self.api.paged_mqa_logits(d["q"], d["weights"], d["kv"], d["block_table"], d["visible"],
                                   page_cols=s.page_cols, out_cols=s.out_cols, kv_dtype=s.kv_dtype,
                                   scale_offset=self.inp.scale_offset, out=d["out"], next_n_lens=d.get("next_n_lens"))
+
+    def stream(self, d):
+        """The page-stream reference: the scorer's pages, read and discarded."""
+        self.api.page_stream(d["kv"], self.inp.key_page_stride, self.page_bytes, d["pages"], checksum=d["pcheck"])
 
     def topk(self, d):  # ragged call: the top-k reads the live rows' visible counts
         self.api.select_topk(d["out"], d.get("visible_live", d["visible"]), self.spec.k, out=d["idx"])
@@ -448,6 +463,8 @@ class Workload:
                 d = self.sets[i % self.copies]
                 if what == "score":
                     self.score(d)
+                elif what == "stream":
+                    self.stream(d)
                 elif what == "topk":
                     self.topk(d)
                 else:
@@ -492,6 +509,12 @@ class Workload:
             g = self.capture(n, what)
             out[key] = stats(self.time_graph(g, n, reps))
             del g
+        if self.page_list.size:  # the same pages, streamed with no arithmetic
+            self.stream(self.sets[0])
+            torch.cuda.synchronize(self.dev)
+            g = self.capture(n, "stream")
+            out["page_stream_us"] = stats(self.time_graph(g, n, reps))
+            del g
         # the one call with the selection inside the scoring kernel (forced;
         # the dispatch takes the two launches), where that kernel serves the shape
         qsa.force_variant(qsa.VARIANT_UMMA_TOPK)
@@ -521,6 +544,12 @@ class Workload:
              "topk_gbs": round(sum(tb.values()) / t_topk / 1e9, 1),
              "topk_frac": round(sum(tb.values()) / t_topk / 1e9 / peaks["hbm_gbs"], 4),
              "topk_us_per_row": round(ks["topk_us"]["median"] / spec.num_rows, 4)}
+        if "page_stream_us" in ks:
+            t_stream = ks["page_stream_us"]["median"] * 1e-6
+            sbytes = self.page_list.size * self.page_bytes
+            e["page_stream_gbs"] = round(sbytes / t_stream / 1e9, 1)
+            e["page_stream_frac"] = round(sbytes / t_stream / 1e9 / peaks["hbm_gbs"], 4)
+            e["scoring_vs_page_stream"] = round(t_stream / t_score, 4)
         flops = 2 * spec.head_dim * spec.num_heads * int(spec.live_visible().astype(np.int64).sum())
         if spec.rows_per_req > 64:  # the contraction-heavy case: tensor-core rate too
             e["mma_tflops"] = round(flops / t_score / 1e12, 1)
@@ -622,6 +651,12 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                 "algorithmic_bytes": int(kbytes), "peak_source": f"{peaks['source']} (copy bandwidth)",
                 "key_bytes_frac": head["frac_key_bytes"] if kname != "topk" else None}
+    if kname != "topk" and "page_stream_gbs" in head:
+        # the achievable side: the scorer's pages streamed with no arithmetic
+        # (qsa_page_stream), and the scoring call's time against it
+        roofline["page_stream"] = {"achieved": head["page_stream_gbs"], "unit": "GB/s",
+                                   "frac_of_peak": head["page_stream_frac"],
+                                   "scoring_frac_of_stream": head["scoring_vs_page_stream"]}
 
     # end to end through the public API with host buffers: H2D of every input
     # from pinned memory, both calls, D2H of the top-k indices, every step

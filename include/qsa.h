@@ -330,13 +330,42 @@ const char* qsa_last_error(void);
  * scoring kernel gave up waiting on one of its internal barriers (about one
  * second): that launch left its output incomplete and returned early instead
  * of hanging the GPU.  Bit 1: a top-k launch gave up waiting for its row copy
- * (its selection for that row is unspecified).  Synchronises the current
+ * (its selection for that row is unspecified).  Bit 2: a qsa_page_stream
+ * launch gave up waiting for a page (its checksum is unspecified).  Synchronises the current
  * device, then writes the word to *flags (host pointer).  When `clear` is
  * non-zero it then clears the word and zeroes the counter array of
  * qsa_paged_mqa_topk_noalloc on the current device (synchronously), so the
  * next no-alloc call starts clean after a failed one.
  */
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear);
+
+/*
+ * qsa_page_stream - measurement, not part of the scoring path: streams the
+ * listed pages from device memory into shared memory the way the scorers
+ * fetch a request's key pages (one copy per page, in list order, one CTA per
+ * SM taking a contiguous share), with no arithmetic on them, so the time of
+ * a launch is the rate HBM delivers that gather - the achievable side of the
+ * roofline of the key-cache reads that the paged scoring of vLLM #62589
+ * "Overview" (keys gathered through a per-request block table) makes.
+ *
+ *   base        device pointer to pool_pages pages, page p at base + p * page_stride
+ *               (16-byte aligned); read only.
+ *   page_stride bytes from one page to the next (a multiple of 16).
+ *   page_bytes  bytes copied from the start of each listed page: a multiple of
+ *               16 in 16 .. 65536, at most page_stride.
+ *   pages       device int32 [num_listed]: page indices; one outside
+ *               [0, pool_pages) is clamped into it (no fault).
+ *   checksum    device uint32, XORed with the XOR of every 32-bit word of every
+ *               listed page copy (a page listed twice cancels): zero it first
+ *               to read the checksum of one launch.  Written only by this call.
+ *   stream      cudaStream_t (NULL: the legacy default stream); asynchronous.
+ *
+ * Returns QSA_ERR_INVALID_ARG for a null pointer with num_listed > 0, a
+ * misaligned base or stride, page_bytes or pool_pages out of range;
+ * QSA_ERR_CUDA when the launch fails.  num_listed == 0 launches nothing.
+ */
+qsa_status qsa_page_stream(const void* base, int64_t page_stride, int32_t page_bytes, const int32_t* pages,
+                           int64_t num_listed, int64_t pool_pages, uint32_t* checksum, void* stream);
 
 /* QSA_ABI_VERSION of the loaded library. */
 int32_t qsa_abi_version(void);

@@ -26,7 +26,8 @@ EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mq
             "qsa_paged_mqa_topk_workspace", "qsa_paged_mqa_topk_noalloc",
             "qsa_paged_mqa_topk_noalloc_counters", "qsa_select_topk", "qsa_plan_variant",
             "qsa_plan_variant_ex", "qsa_force_variant",
-            "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status")
+            "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status",
+            "qsa_page_stream")
 
 
 class QSAError(RuntimeError):
@@ -96,6 +97,9 @@ def load_library():
                                                             ctypes.POINTER(ctypes.c_size_t)]
         lib.qsa_device_status.restype = ctypes.c_int
         lib.qsa_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        lib.qsa_page_stream.restype = ctypes.c_int
+        lib.qsa_page_stream.argtypes = [ctypes.c_void_p, ctypes.c_int64, i32, ctypes.c_void_p, ctypes.c_int64,
+                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
         _lib = lib
     return _lib
 
@@ -192,6 +196,13 @@ def select_topk(logits, num_rows: int, row_stride: int, visible_cols, k: int, ou
     st = load_library().qsa_select_topk(_addr(logits), int(num_rows), int(row_stride), _addr(visible_cols),
                                         int(k), _addr(out_idx), _stream(stream))
     _check(st)
+
+
+def page_stream(base, page_stride: int, page_bytes: int, pages, num_listed: int, pool_pages: int, checksum,
+                stream=None) -> None:
+    """qsa_page_stream (include/qsa.h): the measurement stream of listed pages."""
+    _check(load_library().qsa_page_stream(_addr(base), int(page_stride), int(page_bytes), _addr(pages),
+                                          int(num_listed), int(pool_pages), _addr(checksum), _stream(stream)))
 
 
 def plan_variant(desc: PagedDesc, q_dtype: int | None = None) -> int:

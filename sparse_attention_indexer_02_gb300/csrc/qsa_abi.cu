@@ -414,6 +414,24 @@ qsa_status qsa_paged_mqa_topk_noalloc_counters(void** device_ptr, size_t* bytes)
   return QSA_OK;
 }
 
+qsa_status qsa_page_stream(const void* base, int64_t page_stride, int32_t page_bytes, const int32_t* pages,
+                           int64_t num_listed, int64_t pool_pages, uint32_t* checksum, void* stream) {
+  if (num_listed < 0) return fail(QSA_ERR_INVALID_ARG, "num_listed < 0");
+  if (num_listed == 0) return QSA_OK;
+  if (!base || !pages || !checksum) return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(base) % 16 != 0 || page_stride % 16 != 0 || page_stride < 16)
+    return fail(QSA_ERR_INVALID_ARG, "base and page_stride must be multiples of 16 bytes");
+  if (page_bytes < 16 || page_bytes > 65536 || page_bytes % 16 != 0 || page_bytes > page_stride)
+    return fail(QSA_ERR_INVALID_ARG, "page_bytes must be a multiple of 16 in 16..65536 and at most page_stride");
+  if (pool_pages < 1) return fail(QSA_ERR_INVALID_ARG, "pool_pages < 1");
+  if (reinterpret_cast<uintptr_t>(pages) % 4 != 0 || reinterpret_cast<uintptr_t>(checksum) % 4 != 0)
+    return fail(QSA_ERR_INVALID_ARG, "pages and checksum must be 4-byte aligned");
+  cudaError_t e = qsa::launch_page_stream(static_cast<const uint8_t*>(base), page_stride, page_bytes, pages,
+                                          num_listed, pool_pages, checksum, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "page stream launch: %s", cudaGetErrorString(e));
+  return QSA_OK;
+}
+
 qsa_status qsa_device_status(uint32_t* flags, int32_t clear) {
   if (!flags) return fail(QSA_ERR_INVALID_ARG, "flags is NULL");
   cudaError_t e = qsa::read_fault_word(flags, clear != 0);

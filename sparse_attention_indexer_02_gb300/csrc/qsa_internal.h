@@ -66,4 +66,8 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* info);
 
+// page_stream.cu: qsa_page_stream's launch (arguments already validated).
+cudaError_t launch_page_stream(const uint8_t* base, int64_t page_stride, int32_t page_bytes, const int32_t* pages,
+                               int64_t num_listed, int64_t pool_pages, uint32_t* checksum, cudaStream_t stream);
+
 }  // namespace qsa

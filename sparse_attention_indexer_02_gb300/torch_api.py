@@ -65,6 +65,17 @@ def select_topk(logits: torch.Tensor, visible_cols: torch.Tensor, k: int,
     return out
 
 
+def page_stream(pool: torch.Tensor, page_stride: int, page_bytes: int, pages: torch.Tensor,
+                checksum: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Stream the listed pages of `pool` (a device buffer of whole pages) and
+    XOR their 32-bit words into `checksum` (include/qsa.h, qsa_page_stream)."""
+    if checksum is None:
+        checksum = torch.zeros(1, dtype=torch.int32, device=pool.device)
+    pool_pages = pool.numel() * pool.element_size() // page_stride
+    _abi.page_stream(pool, page_stride, page_bytes, pages, pages.numel(), pool_pages, checksum, stream)
+    return checksum
+
+
 _workspaces: dict = {}
 
 
