@@ -16,6 +16,13 @@ using namespace sel;
 
 constexpr int kT = 512;  // threads per CTA
 constexpr int kW = kT / 32;
+// The narrow form: 256 threads and at most kNarrowSmem of shared memory, so
+// that four CTAs (four rows) share an SM, for launches of many rows longer
+// than the register path's 8192 columns.  A row's phases (sample, pass,
+// candidate select) are latency-bound, so more rows in flight an SM pay
+// more than more threads a row.
+constexpr int kTn = 256;
+constexpr int64_t kNarrowSmem = 55 * 1024;
 constexpr int64_t kSmemMax = 226 * 1024;  // dynamic shared memory per CTA (static part aside)
 constexpr int kRegKeys = 16;              // keys per thread of the register path (rows <= 8192)
 
@@ -35,8 +42,8 @@ struct TopkArgs {
   int32_t pcap;  // candidates of the sampled-pivot path (0: off)
 };
 
-template <bool CLUSTER>
-__global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
+template <bool CLUSTER, int NT>
+__global__ void __launch_bounds__(NT, NT == kT ? 2 : 4) topk_kernel(const TopkArgs a) {
   extern __shared__ uint4 dyn_topk[];
   __shared__ Shared sh;
   int CL = 1, rank = 0;  // cluster size and this CTA's rank in it
@@ -55,7 +62,7 @@ __global__ void __launch_bounds__(kT, 2) topk_kernel(const TopkArgs a) {
   ptx::grid_dep_launch();
   const RowTask task{a.logits + row * a.row_stride, n, a.out + row * (int64_t)a.k};
   const Config cf{a.k, a.cap, a.cpw, a.bulk, a.fault, a.pcap};
-  select_row<kT, CLUSTER, false, kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh, CL, rank);
+  select_row<NT, CLUSTER, false, kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh, CL, rank);
 }
 
 }  // namespace
@@ -123,7 +130,7 @@ cudaError_t max_active_clusters(int c, size_t smem, int* out) {
       *out = cache[i].n;
       return cudaSuccess;
     }
-  e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(topk_kernel<true, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)c, 1, 1);
@@ -137,7 +144,7 @@ cudaError_t max_active_clusters(int c, size_t smem, int* out) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, topk_kernel<true>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, topk_kernel<true, kT>, &cfg);
   if (e != cudaSuccess) return e;
   cache[used % 32] = Entry{dev, c, smem, n};
   if (used < 32) ++used;
@@ -171,7 +178,20 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   DeviceInfo dinfo;
   e = device_info(&dinfo);
   if (e != cudaSuccess) return e;
-  const TopkPlan pl = plan_for(C, row_stride, num_rows > dinfo.num_sms);
+  // many rows, longer than the register path: the narrow form (its plan: the
+  // histograms, 256-entry candidate lists, the rest a partial row cache)
+  const bool narrow = C == 1 && row_stride > (int64_t)kT * kRegKeys && num_rows > 2 * (int64_t)dinfo.num_sms;
+  const int nt = narrow ? kTn : kT;
+  TopkPlan pl = plan_for(C, row_stride, num_rows > dinfo.num_sms);
+  if (narrow) {
+    const int64_t fixed = 4LL * kBins, cpw = 256;
+    int64_t cap = ((kNarrowSmem - fixed - 4LL * (kTn / 32) * cpw) / 4) & ~int64_t(3);
+    const int64_t per_row = (row_stride + 3) & ~int64_t(3);
+    if (cap > per_row) cap = per_row;
+    size_t bytes = (size_t)(4 * (cap + (kTn / 32) * cpw) + fixed);
+    const size_t reg = 4 * (size_t)kRegHistWords;
+    pl = TopkPlan{cap, cpw, bytes > reg ? bytes : reg};
+  }
   TopkArgs a;
   a.logits = logits;
   a.row_stride = row_stride;
@@ -186,12 +206,12 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   a.cpw = (int32_t)pl.cpw;
   // the sampled-pivot path's candidate columns after its histograms
   const int64_t pc = (int64_t)pl.smem / 4 - kRegHistWords;
-  a.pcap = (int32_t)((pc < kT * kRegKeys ? pc : kT * kRegKeys) & ~int64_t(3));
+  a.pcap = (int32_t)((pc < (int64_t)nt * kRegKeys ? pc : (int64_t)nt * kRegKeys) & ~int64_t(3));
   // segment starts are multiples of 4 columns: 16-byte aligned when rows are
   a.bulk = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (row_stride & 3) == 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(num_rows * C), 1, 1);
-  cfg.blockDim = dim3(kT, 1, 1);
+  cfg.blockDim = dim3(nt, 1, 1);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -204,13 +224,17 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   cfg.attrs = attr;
   cfg.numAttrs = C > 1 ? 2 : 1;
   if (C > 1) {
-    e = cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    e = cudaFuncSetAttribute(topk_kernel<true, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel<true>, a);
+    e = cudaLaunchKernelEx(&cfg, topk_kernel<true, kT>, a);
+  } else if (narrow) {
+    e = cudaFuncSetAttribute(topk_kernel<false, kTn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    if (e != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, topk_kernel<false, kTn>, a);
   } else {
-    e = cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+    e = cudaFuncSetAttribute(topk_kernel<false, kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, topk_kernel<false>, a);
+    e = cudaLaunchKernelEx(&cfg, topk_kernel<false, kT>, a);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

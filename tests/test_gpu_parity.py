@@ -529,11 +529,12 @@ def test_topk_threshold_bin_taken_whole(oracle_mod, n):
     assert sorted(idx[0].tolist()) == np.flatnonzero(x[0] >= 1.0).tolist()
 
 
-@pytest.mark.parametrize("rows,n", [(4, 16000), (200, 22528), (160, 65537)])
+@pytest.mark.parametrize("rows,n", [(4, 16000), (200, 22528), (160, 65537), (400, 22528)])
 def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
     """Rows one CTA selects alone and longer than its keys-in-registers limit
     (4 rows of 16000 columns, 200 of 22528, 160 of 65537 - sampled more
-    sparsely): a sample of every 8th block of 128 columns sets a threshold, the
+    sparsely - and 400 of 22528, more rows than twice the SMs: the narrow
+    256-thread form): a sample of every 8th block of 128 columns sets a threshold, the
     exact selection runs on the candidates above it.  Continuous values, then every sampled block raised far above
     the rest (the sample's threshold lets fewer than k columns through, so the
     full path must take over), then exact zeros spanning the k-th place (the
@@ -557,9 +558,10 @@ def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
 
 
 def test_topk_more_rows_than_resident_ctas(oracle_mod):
-    """More rows than the device holds CTAs at once, mixing every path a row
-    can take: at most k columns, keys in registers, the sampled pivot, and
-    its fallback (all values equal)."""
+    """More rows than the device holds CTAs at once (the narrow 256-thread form,
+    whose register path ends at 4096 columns), mixing every path a row can
+    take: at most k columns, keys in registers, the sampled pivot, and its
+    fallback (all values equal)."""
     rows, width, k = 700, 12000, 1024
     rng = np.random.default_rng(700)
     vis = rng.integers(9000, width + 1, size=rows).astype(np.int32)
