@@ -204,8 +204,8 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   a.k = k;
   a.cap = (int32_t)pl.cap;
   a.cpw = (int32_t)pl.cpw;
-  // the sampled-pivot path's candidate columns after its histograms
-  const int64_t pc = (int64_t)pl.smem / 4 - kRegHistWords;
+  // the sampled-pivot path's candidates after its histograms: a column and a key each
+  const int64_t pc = ((int64_t)pl.smem / 4 - kRegHistWords) / 2;
   a.pcap = (int32_t)((pc < (int64_t)nt * kRegKeys ? pc : (int64_t)nt * kRegKeys) & ~int64_t(3));
   // segment starts are multiples of 4 columns: 16-byte aligned when rows are
   a.bulk = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && (row_stride & 3) == 0;

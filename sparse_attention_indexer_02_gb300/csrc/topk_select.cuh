@@ -79,7 +79,7 @@ struct Config {
   int cpw;    // candidate list entries per warp (multiple of 4)
   int bulk;   // segments start 16-byte aligned: bulk copies fill the cache
   unsigned int* fault;  // bit 1 set when a copy wait gives up
-  int pcap;   // candidate columns the sampled-pivot path holds (<= NT * KPT; below k: path off)
+  int pcap;   // candidates (a column and a key each) the sampled-pivot path holds (<= NT * KPT; below k: off)
 };
 
 // Dynamic shared memory one selecting CTA needs (bytes).
@@ -271,10 +271,10 @@ __device__ __forceinline__ void cluster_sum(const uint32_t* hist, uint32_t* acc,
 constexpr int kRegHistWords = 2 * kBins + 1024;
 
 // CAND: the n keys are those of the sampled-pivot path's candidates, whose
-// columns are in the per-warp slices of `wcap` entries of ccol; slice w holds
-// the candidates from order position sh.weq[w] on (order = column order).
-// Their logits are read again from the row; the selected columns are the
-// candidates' ccol entries.
+// columns are in the per-warp slices of `wcap` entries of ccol and whose keys
+// are at the same places of the NT / 32 slices that follow them; slice w
+// holds the candidates from order position sh.weq[w] on (order = column
+// order).  The selected columns are the candidates' ccol entries.
 template <int NT, int KPT, bool COHERENT, bool CLUSTER, bool CAND = false>
 __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config& cf, uint32_t* dyn, Shared& sh,
                                                int C, int part, const int32_t* ccol = nullptr, int wcap = 0) {
@@ -322,12 +322,10 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
         cidx[j] = w * wcap + (c0 + j - lo);
       }
     }
-    // then every logit load at once (independent of one another)
-    float v[KPT];
+    // their keys, written by the pivot pass beside their columns
+    const uint32_t* ckey = reinterpret_cast<const uint32_t*>(ccol) + kWs * wcap;
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) v[j] = j < mine ? ld_row1<COHERENT>(task.row + ccol[cidx[j]]) : 0.0f;
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) key[j] = j < mine ? topk_key(v[j]) : 0u;
+    for (int j = 0; j < KPT; ++j) key[j] = j < mine ? ckey[cidx[j]] : 0u;
   } else if ((q & 3) == 0 && (reinterpret_cast<uintptr_t>(x + c0) & 15u) == 0) {
 #pragma unroll
     for (int j = 0; j < KPT; j += 4) {
@@ -454,17 +452,19 @@ __device__ __forceinline__ void select_row_reg(const RowTask& task, const Config
 //     22-bit key bin holding the sample's j-th largest key, j the k-th
 //     place scaled to the sample plus four standard deviations and 16.
 //  2. One pass over the row (each warp a contiguous segment, each lane 16
-//     consecutive columns a step) writes the columns at or above T into the
-//     warp's own slice of shared memory, in column order (a lane's offset
-//     from one scan of its candidate count, its stores one per set bit).
+//     consecutive columns a step) writes the columns at or above T, and
+//     their keys, into the warp's own slices of shared memory, in column
+//     order (a lane's offset from one scan of its candidate count, its stores
+//     one per set bit).
 //  3. The exact selection runs on the candidates alone, keys in registers
-//     (select_row_reg reading the warps' slices in order, each candidate's
-//     logit again from L2), and writes the selected candidates' columns.
+//     (select_row_reg reading the warps' slices in order), and writes the
+//     selected candidates' columns.  (Reading each candidate's logit again
+//     from L2 instead cost ~5 us a row.)
 // It gives up - the caller then runs the full path - when fewer than k
 // columns reach T (every selected key must be a candidate) or a warp's slice
 // overflows; the decisions read shared values, so every thread takes the
 // same one.  Shared memory at `dyn`: the three histograms (kRegHistWords),
-// then per warp `wcap` candidate columns.
+// then per warp `wcap` candidate columns, then per warp `wcap` their keys.
 
 // The smallest float whose key (topk_key) is at least tk, for the compare
 // x >= T on floats: -inf below every finite key, NaN above them (no float
@@ -489,6 +489,7 @@ __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Conf
   uint32_t* h0 = dyn;
   uint32_t* h1 = h0 + kBins;
   int32_t* scol = reinterpret_cast<int32_t*>(dyn + kRegHistWords) + warp * wcap;  // this warp's slice
+  uint32_t* skey = dyn + kRegHistWords + kW * wcap + warp * wcap;                  // and its keys
   // four columns c..c+3 (c a multiple of 4) up to `end`; past it NaN, which
   // compares false with every threshold
   auto load4 = [&](int c, int end) -> float4 {
@@ -582,7 +583,13 @@ __device__ __forceinline__ bool select_row_pivot(const RowTask& task, const Conf
     while (m) {
       const int i = __ffs(m) - 1;
       m &= m - 1u;
-      if (pos < wcap) scol[pos] = c + i;
+      if (pos < wcap) {
+        // the value at column c + i, picked by selects (no indexed registers)
+        const float4 fv = (i >> 2) == 0 ? f[0] : ((i >> 2) == 1 ? f[1] : ((i >> 2) == 2 ? f[2] : f[3]));
+        const float val = (i & 3) == 0 ? fv.x : ((i & 3) == 1 ? fv.y : ((i & 3) == 2 ? fv.z : fv.w));
+        scol[pos] = c + i;
+        skey[pos] = topk_key(val);
+      }
       ++pos;
     }
     ncw += __shfl_sync(0xFFFFFFFFu, incl, 31);

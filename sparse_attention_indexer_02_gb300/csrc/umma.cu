@@ -284,8 +284,8 @@ cudaError_t launch_umma(const ScoreParams& p, cudaStream_t stream, const char** 
     up.topk_k = fuse->k;
     up.topk_cap = (int32_t)cap;
     up.topk_cpw = cpw;
-    // the sampled-pivot path's candidate columns after its histograms
-    const int64_t pc = ((int64_t)L.bar_off - kSelSharedBytes) / 4 - sel::kRegHistWords;
+    // the sampled-pivot path's candidates after its histograms: a column and a key each
+    const int64_t pc = (((int64_t)L.bar_off - kSelSharedBytes) / 4 - sel::kRegHistWords) / 2;
     const int64_t pmax = (int64_t)nt * kFuseKeys;
     up.topk_pcap = (int32_t)((pc < pmax ? pc : pmax) & ~int64_t(3));
     if (kind == kKindFp8Q) return launch_q8_topk(p.num_heads, kv_map, q_map, up, L, grid, stream);
