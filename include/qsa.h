@@ -59,7 +59,7 @@ extern "C" {
 typedef enum qsa_status {
   QSA_OK = 0,
   QSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or stride */
-  QSA_ERR_UNSUPPORTED = 2, /* valid request this build cannot serve (e.g. head_dim != 128) */
+  QSA_ERR_UNSUPPORTED = 2, /* valid request this library cannot serve (e.g. head_dim != 128) */
   QSA_ERR_CUDA = 3         /* a CUDA runtime call or kernel launch failed */
 } qsa_status;
 
