@@ -529,6 +529,43 @@ def test_topk_threshold_bin_taken_whole(oracle_mod, n):
     assert sorted(idx[0].tolist()) == np.flatnonzero(x[0] >= 1.0).tolist()
 
 
+KEY_SPANS = [1, 2, 2047, 2048, 2049, 4095, (1 << 22) - 1, 1 << 22, (1 << 22) + 1, (1 << 24) + 3, None]
+
+
+def key_span_rows(rng, rows, n):
+    """Rows of n columns whose order-preserving keys cover exactly KEY_SPANS[r]
+    (row r cycles through them): float32 bit patterns 1.0 + offsets in
+    [0, span] with both ends present, so small spans hold many equal values;
+    None is a row of both signs from -1e30 to 1e30 (a span near 2^32)."""
+    x = np.empty((rows, n), np.float32)
+    for r in range(rows):
+        span = KEY_SPANS[r % len(KEY_SPANS)]
+        if span is None:
+            v = rng.uniform(-1e30, 1e30, n).astype(np.float32)
+            v[rng.integers(n)], v[rng.integers(n)] = np.float32(-1e30), np.float32(1e30)
+        else:
+            off = rng.integers(0, span + 1, n, dtype=np.int64)
+            off[rng.integers(n)], off[rng.integers(n)] = 0, span
+            v = (np.uint32(0x3F800000) + off.astype(np.uint32)).view(np.float32)
+        x[r] = v
+    return x
+
+
+@pytest.mark.parametrize("rows,n", [(11, 8192), (11, 5001), (200, 22528)])
+def test_topk_key_spans_at_the_digit_boundaries(oracle_mod, rows, n):
+    """One CTA a row takes its digits from the keys' offsets above the smallest
+    one, as many bits as the span needs: spans below 2048 end after one digit,
+    below 2^22 after two, the rest take three; the rows put the span on each
+    side of those boundaries (the register path for 8192 and 5001 columns, the
+    sampled pivot's candidate select for 22528)."""
+    rng = np.random.default_rng(n)
+    x = key_span_rows(rng, rows, n)
+    vis = np.full(rows, n, np.int32)
+    for k in (2048, 1):
+        idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k)
+        assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+
+
 @pytest.mark.parametrize("rows,n", [(4, 16000), (200, 22528), (160, 65537), (400, 22528)])
 def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
     """Rows one CTA selects alone and longer than its keys-in-registers limit
