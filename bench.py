@@ -1,9 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark of the QSA-indexer hot path: paged MQA-logits scoring + top-k.
 
-One step = qsa_paged_mqa_logits + qsa_select_topk over one batch of the
-workload (two kernel launches; with --step fused one qsa_paged_mqa_topk
-call).  Prints one JSON line.
+One step = qsa_paged_mqa_logits + qsa_select_topk_bounded (the batch's
+longest visible count as the host bound) over one batch of the workload (two
+kernel launches; with --step fused one qsa_paged_mqa_topk call).  Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -435,8 +436,11 @@ class Workload:
         """The page-stream reference: the scorer's pages, read and discarded."""
         self.api.page_stream(d["kv"], self.inp.key_page_stride, self.page_bytes, d["pages"], checksum=d["pcheck"])
 
-    def topk(self, d):  # ragged call: the top-k reads the live rows' visible counts
-        self.api.select_topk(d["out"], d.get("visible_live", d["visible"]), self.spec.k, out=d["idx"])
+    def topk(self, d):
+        # the ragged call's top-k reads the live rows' visible counts; the
+        # batch's longest one is the host bound (qsa_select_topk_bounded)
+        self.api.select_topk(d["out"], d.get("visible_live", d["visible"]), self.spec.k, out=d["idx"],
+                             max_visible=self.max_visible)
 
     def one_call(self, d):
         # qsa_paged_mqa_topk; the host bound of the visible counts steers its
@@ -761,7 +765,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=sorted(qi.WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", choices=["auto", "rowcore", "umma", "lean"], default="auto")
     ap.add_argument("--step", choices=["two-call", "fused"], default="two-call",
-                    help="time the step as qsa_paged_mqa_logits + qsa_select_topk, or as one qsa_paged_mqa_topk")
+                    help="time the step as qsa_paged_mqa_logits + qsa_select_topk_bounded, or as one qsa_paged_mqa_topk")
     ap.add_argument("--no-rotate", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -201,6 +201,30 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
                            void* stream);
 
 /*
+ * qsa_select_topk_bounded - qsa_select_topk with the caller's host bound on
+ * the visible counts.
+ *
+ * A serving host knows the longest context of its batch (SGLang #48649's
+ * test body hands max_model_len to the scorer beside context_lens; vLLM
+ * #62589 "Dispatch" picks its decode path from host metadata).  Given it,
+ * each row's count is clamped to [0, min(max_visible, row_stride)] instead
+ * of [0, row_stride]; everything else is as qsa_select_topk.  A row whose
+ * visible_cols[r] exceeds the bound therefore selects from its first
+ * max_visible columns only: the bound is a capacity, not a hint.
+ * max_visible <= 0 means no bound (exactly qsa_select_topk).
+ *
+ * With a bound of at most 8192 columns every row is selected by one CTA of
+ * 1024 threads holding the row's keys in registers (faster for decode rows
+ * than the general form, which must allow rows of any length).
+ *
+ * Arguments as qsa_select_topk, plus max_visible (host value).  Errors as
+ * qsa_select_topk.
+ */
+qsa_status qsa_select_topk_bounded(const float* logits, int64_t num_rows, int64_t row_stride,
+                                   const int32_t* visible_cols, int64_t max_visible, int32_t k,
+                                   int32_t* out_idx, void* stream);
+
+/*
  * qsa_paged_mqa_topk - qsa_paged_mqa_logits_ex and then the top-k of every row,
  * in one call.
  *

@@ -24,7 +24,7 @@ VARIANT_NAMES = {VARIANT_ROWCORE: "rowcore", VARIANT_UMMA: "umma", VARIANT_UMMA_
 # Every symbol include/qsa.h declares.
 EXPORTED = ("qsa_paged_mqa_logits", "qsa_paged_mqa_logits_ragged", "qsa_paged_mqa_logits_ex", "qsa_paged_mqa_topk",
             "qsa_paged_mqa_topk_workspace", "qsa_paged_mqa_topk_noalloc",
-            "qsa_paged_mqa_topk_noalloc_counters", "qsa_select_topk", "qsa_plan_variant",
+            "qsa_paged_mqa_topk_noalloc_counters", "qsa_select_topk", "qsa_select_topk_bounded", "qsa_plan_variant",
             "qsa_plan_variant_ex", "qsa_force_variant",
             "qsa_last_variant", "qsa_status_string", "qsa_last_error", "qsa_abi_version", "qsa_device_status",
             "qsa_page_stream")
@@ -78,6 +78,8 @@ def load_library():
         lib.qsa_paged_mqa_topk_workspace.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(ctypes.c_size_t)]
         lib.qsa_select_topk.restype = ctypes.c_int
         lib.qsa_select_topk.argtypes = [vp, i64, i64, vp, i32, vp, vp]
+        lib.qsa_select_topk_bounded.restype = ctypes.c_int
+        lib.qsa_select_topk_bounded.argtypes = [vp, i64, i64, vp, i64, i32, vp, vp]
         lib.qsa_plan_variant.restype = ctypes.c_int
         lib.qsa_plan_variant.argtypes = [ctypes.POINTER(PagedDesc), ctypes.POINTER(i32)]
         lib.qsa_plan_variant_ex.restype = ctypes.c_int
@@ -195,6 +197,13 @@ def topk_workspace_bytes(desc: PagedDesc) -> int:
 def select_topk(logits, num_rows: int, row_stride: int, visible_cols, k: int, out_idx, stream=None) -> None:
     st = load_library().qsa_select_topk(_addr(logits), int(num_rows), int(row_stride), _addr(visible_cols),
                                         int(k), _addr(out_idx), _stream(stream))
+    _check(st)
+
+
+def select_topk_bounded(logits, num_rows: int, row_stride: int, visible_cols, max_visible: int, k: int, out_idx,
+                        stream=None) -> None:
+    st = load_library().qsa_select_topk_bounded(_addr(logits), int(num_rows), int(row_stride), _addr(visible_cols),
+                                                int(max_visible), int(k), _addr(out_idx), _stream(stream))
     _check(st)
 
 

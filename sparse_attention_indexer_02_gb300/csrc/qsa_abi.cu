@@ -450,6 +450,12 @@ qsa_status qsa_device_status(uint32_t* flags, int32_t clear) {
 
 qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_stride,
                            const int32_t* visible_cols, int32_t k, int32_t* out_idx, void* stream) {
+  return qsa_select_topk_bounded(logits, num_rows, row_stride, visible_cols, 0, k, out_idx, stream);
+}
+
+qsa_status qsa_select_topk_bounded(const float* logits, int64_t num_rows, int64_t row_stride,
+                                   const int32_t* visible_cols, int64_t max_visible, int32_t k, int32_t* out_idx,
+                                   void* stream) {
   if (num_rows < 0) return fail(QSA_ERR_INVALID_ARG, "num_rows < 0");
   if (row_stride < 1) return fail(QSA_ERR_INVALID_ARG, "row_stride < 1");
   if (k < 1 || k > 2048) return fail(QSA_ERR_INVALID_ARG, "k must be in 1..2048 (got %d)", k);
@@ -458,8 +464,9 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
   if (!logits || !visible_cols || !out_idx) return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(logits, 4) || !aligned(visible_cols, 4) || !aligned(out_idx, 4))
     return fail(QSA_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
-  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, nullptr, 1, row_stride, k,
-                                   out_idx, static_cast<cudaStream_t>(stream));
+  const int64_t capacity = max_visible > 0 && max_visible < row_stride ? max_visible : row_stride;
+  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, nullptr, 1, capacity, k, out_idx,
+                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
 }

@@ -23,6 +23,16 @@ constexpr int kW = kT / 32;
 // more than more threads a row.
 constexpr int kTn = 256;
 constexpr int64_t kNarrowSmem = 55 * 1024;
+// The register form: 1024 threads holding 8 keys each, one CTA an SM, for
+// launches of at most two rows an SM whose rows are bounded at kTr *
+// kRegKeysR columns (the capacity: the row stride, or a caller's bound; the
+// decode rows).  A row is one latency-bound chain on one SM (loads, digit
+// histograms, scans, stores); twice the threads halve each thread's part of
+// it (single-row decode top-k 5.78 -> 5.27 us against 512 threads of 16
+// keys).  Only the register path is reachable: the counts are clamped to the
+// bound, and the launch holds the three histograms alone.
+constexpr int kTr = 1024;
+constexpr int kRegKeysR = 8;
 constexpr int64_t kSmemMax = 226 * 1024;  // dynamic shared memory per CTA (static part aside)
 constexpr int kRegKeys = 16;              // keys per thread of the register path (rows <= 8192)
 
@@ -43,7 +53,7 @@ struct TopkArgs {
 };
 
 template <bool CLUSTER, int NT>
-__global__ void __launch_bounds__(NT, NT == kT ? 2 : 4) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(NT, NT == kTr ? 1 : (NT == kT ? 2 : 4)) topk_kernel(const TopkArgs a) {
   extern __shared__ uint4 dyn_topk[];
   __shared__ Shared sh;
   int CL = 1, rank = 0;  // cluster size and this CTA's rank in it
@@ -62,7 +72,8 @@ __global__ void __launch_bounds__(NT, NT == kT ? 2 : 4) topk_kernel(const TopkAr
   ptx::grid_dep_launch();
   const RowTask task{a.logits + row * a.row_stride, n, a.out + row * (int64_t)a.k};
   const Config cf{a.k, a.cap, a.cpw, a.bulk, a.fault, a.pcap};
-  select_row<NT, CLUSTER, false, kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh, CL, rank);
+  select_row<NT, CLUSTER, false, NT == kTr ? kRegKeysR : kRegKeys>(task, cf, reinterpret_cast<uint32_t*>(dyn_topk), sh,
+                                                                   CL, rank);
 }
 
 }  // namespace
@@ -152,6 +163,46 @@ cudaError_t max_active_clusters(int c, size_t smem, int* out) {
   return cudaSuccess;
 }
 
+// The register form (kTr threads, kRegKeysR keys each): every row's count
+// is clamped to cap_cols <= kTr * kRegKeysR, so every row takes the register
+// path; the launch holds only its three histograms, with no cache, candidate
+// lists or pivot candidates (each sized 0: the other paths, never reached,
+// would stay inside the allocation).
+cudaError_t launch_register_form(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
+                                 const int32_t* next_n_lens, int32_t rows_per_req, int64_t cap_cols, int32_t k,
+                                 int32_t* out, unsigned int* fault, cudaStream_t stream) {
+  TopkArgs a;
+  a.logits = logits;
+  a.row_stride = row_stride;
+  a.visible = visible;
+  a.next_n_lens = next_n_lens;
+  a.capacity = cap_cols;
+  a.rows_per_req = rows_per_req;
+  a.out = out;
+  a.fault = fault;
+  a.k = k;
+  a.cap = 0;
+  a.cpw = 0;
+  a.pcap = 0;
+  a.bulk = 0;
+  const size_t smem = 4 * (size_t)kRegHistWords;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel<false, kTr>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_rows, 1, 1);
+  cfg.blockDim = dim3(kTr, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see grid_dep_wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, topk_kernel<false, kTr>, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
@@ -162,6 +213,15 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   unsigned int* fault = nullptr;
   cudaError_t e = fault_word_address(&fault);
   if (e != cudaSuccess) return e;
+  DeviceInfo dinfo;
+  e = device_info(&dinfo);
+  if (e != cudaSuccess) return e;
+  // Rows of at most kTr * kRegKeysR columns, few enough that each has an SM
+  // to itself or shares it with one other: the register form.
+  const int64_t cap_cols = capacity < row_stride ? capacity : row_stride;  // visible counts are clamped to it
+  if (cap_cols <= (int64_t)kTr * kRegKeysR && num_rows <= 2 * (int64_t)dinfo.num_sms)
+    return launch_register_form(logits, num_rows, row_stride, visible, next_n_lens, rows_per_req, cap_cols, k, out,
+                                fault, stream);
   // Rows that may be longer than kSoloMax columns, and few enough that the
   // device holds all their clusters at once: split over the largest cluster.
   int C = 1;
@@ -175,9 +235,6 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
         break;
       }
     }
-  DeviceInfo dinfo;
-  e = device_info(&dinfo);
-  if (e != cudaSuccess) return e;
   // many rows, longer than the register path: the narrow form (its plan: the
   // histograms, 256-entry candidate lists, the rest a partial row cache)
   const bool narrow = C == 1 && row_stride > (int64_t)kT * kRegKeys && num_rows > 2 * (int64_t)dinfo.num_sms;

@@ -52,7 +52,7 @@ constexpr int kSoloMax = 16384;               // rows up to this long: one CTA e
 constexpr int kAccWords = 2 * 2048 + 1024;    // cluster accumulators of the three digits
 constexpr int kSeg = 128;                     // columns a warp covers per step
 constexpr int kMaxCluster = 8;
-constexpr int kMaxWarps = 16;                 // selecting threads per CTA: 256 or 512
+constexpr int kMaxWarps = 32;                 // selecting threads per CTA: 256, 512 or 1024
 constexpr long long kSpinCycles = 2000000000LL;  // ~1 s at 2 GHz
 constexpr int kBarrier = 2;                   // named barrier of the selecting threads
 

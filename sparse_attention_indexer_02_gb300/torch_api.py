@@ -56,12 +56,17 @@ def paged_mqa_logits(q: torch.Tensor, weights: torch.Tensor, kv_cache: torch.Ten
 
 
 def select_topk(logits: torch.Tensor, visible_cols: torch.Tensor, k: int,
-                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """Top-k column indices int32 [rows, k] (include/qsa.h, qsa_select_topk)."""
+                out: Optional[torch.Tensor] = None, stream=None, max_visible: int = 0) -> torch.Tensor:
+    """Top-k column indices int32 [rows, k] (include/qsa.h, qsa_select_topk;
+    with max_visible > 0, qsa_select_topk_bounded: the visible counts are
+    clamped to that host bound)."""
     rows = logits.shape[0]
     if out is None:
         out = torch.empty((rows, k), dtype=torch.int32, device=logits.device)
-    _abi.select_topk(logits, rows, logits.stride(0), visible_cols, k, out, stream)
+    if max_visible > 0:
+        _abi.select_topk_bounded(logits, rows, logits.stride(0), visible_cols, max_visible, k, out, stream)
+    else:
+        _abi.select_topk(logits, rows, logits.stride(0), visible_cols, k, out, stream)
     return out
 
 

@@ -110,6 +110,8 @@ def test_empty_calls_are_no_ops(lib):
     qsa.paged_mqa_logits(_desc(num_requests=0), None, None, None, None, None, None, None, stream=0)
     qsa.paged_mqa_logits(_desc(out_cols=0), None, None, None, None, None, None, None, stream=0)
     qsa.select_topk(None, 0, 10, None, 8, None, stream=0)
+    for bound in (0, -5, 1, 8192, 1 << 40):
+        qsa.select_topk_bounded(None, 0, 10, None, bound, 8, None, stream=0)
 
 
 @pytest.mark.parametrize("k", [0, -1, 2049])
@@ -117,14 +119,32 @@ def test_topk_k_range(lib, k):
     with pytest.raises(qsa.QSAError) as e:
         qsa.select_topk(16, 4, 100, 16, k, 16, stream=0)
     assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.select_topk_bounded(16, 4, 100, 16, 64, k, 16, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
 
 
-def test_topk_argument_checks(lib):
-    for args in [(16, -1, 100, 16, 8, 16), (16, 4, 0, 16, 8, 16), (None, 4, 100, 16, 8, 16),
-                 (18, 4, 100, 16, 8, 16)]:
-        with pytest.raises(qsa.QSAError) as e:
-            qsa.select_topk(*args, stream=0)
-        assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+TOPK_BAD_ARGS = [(16, -1, 100, 16, 8, 16), (16, 4, 0, 16, 8, 16), (None, 4, 100, 16, 8, 16),
+                 (18, 4, 100, 16, 8, 16), (16, 4, 100, None, 8, 16), (16, 4, 100, 16, 8, None),
+                 (16, 4, 100, 18, 8, 16), (16, 4, 100, 16, 8, 18)]
+
+
+@pytest.mark.parametrize("args", TOPK_BAD_ARGS)
+def test_topk_argument_checks(lib, args):
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.select_topk(*args, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("bound", [0, 100, 8192, 1 << 40])
+@pytest.mark.parametrize("args", TOPK_BAD_ARGS)
+def test_bounded_topk_argument_checks(lib, args, bound):
+    """qsa_select_topk_bounded rejects what qsa_select_topk rejects, whatever
+    the bound (which is never itself an error)."""
+    logits, rows, stride, vis, k, out = args
+    with pytest.raises(qsa.QSAError) as e:
+        qsa.select_topk_bounded(logits, rows, stride, vis, bound, k, out, stream=0)
+    assert e.value.status == qsa.QSA_ERR_INVALID_ARG
 
 
 def test_last_error_names_the_problem(lib):

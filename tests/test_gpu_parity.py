@@ -70,9 +70,9 @@ def gpu_logits(inp, variant=qsa.VARIANT_AUTO, dev=None, stream=None):
     return out, ran, d
 
 
-def gpu_topk(logits_t, visible_t, k):
+def gpu_topk(logits_t, visible_t, k, max_visible=0):
     idx = nan_filled((logits_t.shape[0], k), torch.int32, "cuda")
-    torch_api.select_topk(logits_t, visible_t, k, out=idx)
+    torch_api.select_topk(logits_t, visible_t, k, out=idx, max_visible=max_visible)
     torch.cuda.synchronize()
     return idx.cpu().numpy()
 
@@ -566,6 +566,81 @@ def test_topk_key_spans_at_the_digit_boundaries(oracle_mod, rows, n):
         assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
 
 
+# --------------------------------------------------------------------------
+# qsa_select_topk_bounded: the caller's bound clamps the visible counts; a
+# bound of at most 8192 columns takes the register form (1024 threads)
+# --------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("k", [1, 7, 256, 2048])
+def test_bounded_topk_register_form_edge_rows(oracle_mod, k):
+    """Rows of 0, 1, k - 1, k, k + 1, 3k + 5 and 8192 visible columns, an
+    all-equal row and a row of -0.0 / +0.0, in a 65,603-column stride (as the
+    decode logits, far wider than the bound) under the bound 8192."""
+    vis = [0, 1, max(k - 1, 0), k, k + 1, 3 * k + 5, 8192, 8192, 8192]
+    width = 65603
+    x = _topk_case(len(vis), width, vis, k, zero_frac=0.2, seed=k + 1)
+    x[7, :8192] = 1.25
+    x[8, :8192:2] = -0.0
+    x[8, 1:8192:2] = 0.0
+    vis_np = np.array(vis, np.int32)
+    idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis_np).cuda(), k, max_visible=8192)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, vis_np, k))
+
+
+@pytest.mark.parametrize("rows,width,bound", [(16, 65600, 8192), (40, 8192, 8192), (320, 4099, 5000),
+                                              (3, 8191, 8191), (5, 1000, 700)])
+def test_bounded_topk_matches_oracle_with_counts_clamped(oracle_mod, rows, width, bound):
+    """Random rows whose counts reach past the bound (and past the stride):
+    the selection is the oracle's over min(visible, bound, width) columns.
+    The widths are not multiples of 4 except two (plain and vector loads);
+    320 rows is more than two an SM (152 SMs), which takes the general form."""
+    rng = np.random.default_rng(rows * 7 + width)
+    vis = rng.integers(0, int(bound * 1.3) + 2, size=rows).astype(np.int32)
+    vis[0] = bound + 5
+    vis[-1] = min(bound, width)
+    x = qi.random_logit_rows(rng, rows, width, np.minimum(vis, width), zero_frac=0.1)
+    k = 2048 if bound > 2048 else 256
+    idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k, max_visible=bound)
+    clamped = np.minimum(np.minimum(vis, bound), width).astype(np.int32)
+    assert_topk_strict(idx, oracle_mod.select_topk(x, clamped, k))
+
+
+def test_bounded_topk_key_spans_and_unaligned_rows(oracle_mod):
+    """The key-span rows under a bound of 8192 columns, with the logits
+    starting one float past a 16-byte boundary and a stride of 8195 floats
+    (every row misaligned: plain loads)."""
+    rng = np.random.default_rng(44)
+    rows, n = 11, 8192
+    x = key_span_rows(rng, rows, n)
+    buf = np.zeros((rows, 8195), np.float32)
+    buf[:, :n] = x
+    flat = torch.from_numpy(np.concatenate([np.zeros(1, np.float32), buf.ravel()])).cuda()
+    xt = flat[1:].view(rows, 8195)
+    vis = np.full(rows, n, np.int32)
+    for k in (2048, 1):
+        idx = gpu_topk(xt, torch.from_numpy(vis).cuda(), k, max_visible=n)
+        assert_topk_strict(idx, oracle_mod.select_topk(buf, vis, k))
+
+
+def test_bounded_topk_without_a_bound_is_the_plain_call():
+    """A bound of 0 (none), or one at or above the stride, gives exactly the
+    plain call's indices, as does a bound above 8192 (the general form)."""
+    rng = np.random.default_rng(9)
+    rows, width = 16, 20000
+    vis = rng.integers(1000, width, size=rows).astype(np.int32)
+    x = qi.random_logit_rows(rng, rows, width, vis, zero_frac=0.05)
+    xt, vt = torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda()
+    ref = gpu_topk(xt, vt, 2048)
+    for bound in (0, -3, width, width + 100, 12000):
+        got = gpu_topk(xt, vt, 2048, max_visible=bound)
+        if bound == 12000:
+            assert (got[vis <= 12000] == ref[vis <= 12000]).all()
+        else:
+            assert (got == ref).all()
+    assert qsa.device_status() == 0
+
+
 @pytest.mark.parametrize("rows,n", [(4, 16000), (200, 22528), (160, 65537), (400, 22528)])
 def test_topk_long_rows_sampled_pivot(oracle_mod, rows, n):
     """Rows one CTA selects alone and longer than its keys-in-registers limit
@@ -650,7 +725,8 @@ def test_full_size_workload_sampled(oracle_mod, name):
     assert_logits_match(sub, ref, spec.kv_dtype, where=f"{name} rows {rows}")
     idx_t = nan_filled((spec.num_rows, spec.k), torch.int32, "cuda")
     vis_live = d.get("visible_live", d["visible"])  # ragged: dead rows select nothing
-    torch_api.select_topk(out, vis_live, spec.k, out=idx_t)
+    # the bench's call: the batch's longest visible count as the host bound
+    torch_api.select_topk(out, vis_live, spec.k, out=idx_t, max_visible=int(spec.live_visible().max()))
     torch.cuda.synchronize()
     idx = idx_t.cpu().numpy()
     # strict top-k on a bounded set of rows (the oracle sorts each row)
