@@ -606,13 +606,15 @@ def run_gpu(args):
     full_graphs, rem = divmod(K, per_graph)
     g_step = W.capture(per_graph, form)
     g_rem = W.capture(rem, form) if rem else None
-    for _ in range(max(1, -(-args.warmup // per_graph))):
-        g_step.replay()
-    torch.cuda.synchronize(dev)
 
     stream = torch.cuda.current_stream(dev)
     sampler = ClockSampler(local) if rank == 0 and not args.no_clocks else None
-    time.sleep(0.3 if sampler else 0.0)
+    time.sleep(0.3 if sampler else 0.0)  # the sampler is up before the last warm-up
+    # warm-up replays of the graph right before the timed region (after the
+    # sampler's start-up, so the GPU has not idled since)
+    for _ in range(max(1, -(-args.warmup // per_graph))):
+        g_step.replay()
+    torch.cuda.synchronize(dev)
     barrier()
     torch.cuda.synchronize(dev)
     t0 = time.time()

@@ -206,16 +206,14 @@ qsa_status qsa_select_topk(const float* logits, int64_t num_rows, int64_t row_st
  *
  * A serving host knows the longest context of its batch (SGLang #48649's
  * test body hands max_model_len to the scorer beside context_lens; vLLM
- * #62589 "Dispatch" picks its decode path from host metadata).  Given it,
- * each row's count is clamped to [0, min(max_visible, row_stride)] instead
- * of [0, row_stride]; everything else is as qsa_select_topk.  A row whose
- * visible_cols[r] exceeds the bound therefore selects from its first
- * max_visible columns only: the bound is a capacity, not a hint.
- * max_visible <= 0 means no bound (exactly qsa_select_topk).
- *
- * With a bound of at most 8192 columns every row is selected by one CTA of
- * 1024 threads holding the row's keys in registers (faster for decode rows
- * than the general form, which must allow rows of any length).
+ * #62589 "Dispatch" picks its decode path from host metadata).  The results
+ * are exactly qsa_select_topk's; max_visible, the caller's bound on the
+ * clamped counts (0 or less: none), only chooses the launch.  With a bound
+ * of at most 8192 columns, and at most two rows an SM, every row is
+ * selected by one CTA of 1024 threads holding the row's keys in registers
+ * (faster for decode rows than the general form, which must allow rows of
+ * any length).  A wrong bound costs speed only: a row longer than it is
+ * still selected exactly, from global memory.
  *
  * Arguments as qsa_select_topk, plus max_visible (host value).  Errors as
  * qsa_select_topk.
@@ -247,11 +245,12 @@ qsa_status qsa_select_topk_bounded(const float* logits, int64_t num_rows, int64_
  *   max_visible  host value: the caller's bound on the visible counts, or 0
  *                (unknown; out_cols and the page capacity bound them).  Like
  *                vLLM #62589's single_row_decode flag it only steers the
- *                dispatch of the forced fused kernel: the selection runs in
- *                the scoring kernel for at most 256 rows whose bound is at
- *                most 16384 columns, and as a separate top-k launch (which
- *                splits long rows over a thread-block cluster) otherwise.  A
- *                wrong bound costs speed only.
+ *                dispatch: the top-k launch's form, as in
+ *                qsa_select_topk_bounded, and with the fused kernel forced,
+ *                the selection runs in the scoring kernel for at most 256 rows
+ *                whose bound is at most 16384 columns, and as a separate top-k
+ *                launch (which splits long rows over a thread-block cluster)
+ *                otherwise.  A wrong bound costs speed only.
  *   out_idx      int32 [R][k] (device), 4-byte aligned.
  *   workspace    device memory of at least qsa_paged_mqa_topk_workspace(desc)
  *                bytes, 4-byte aligned (NULL when that size is 0).  It must

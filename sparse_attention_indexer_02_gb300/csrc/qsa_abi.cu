@@ -352,7 +352,7 @@ qsa_status topk_call(const qsa_paged_desc* d, int32_t q_dtype, const void* q, co
   st = launch_scoring(p, variant, s, nullptr);
   if (st != QSA_OK) return st;
   cudaError_t e = qsa::launch_topk(out_logits, p.num_rows, p.out_cols, visible_cols, next_n_lens, p.rows_per_req,
-                                   p.capacity, k, out_idx, s);
+                                   p.capacity, max_visible, k, out_idx, s);
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
 }
@@ -464,9 +464,8 @@ qsa_status qsa_select_topk_bounded(const float* logits, int64_t num_rows, int64_
   if (!logits || !visible_cols || !out_idx) return fail(QSA_ERR_INVALID_ARG, "a required pointer is NULL");
   if (!aligned(logits, 4) || !aligned(visible_cols, 4) || !aligned(out_idx, 4))
     return fail(QSA_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
-  const int64_t capacity = max_visible > 0 && max_visible < row_stride ? max_visible : row_stride;
-  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, nullptr, 1, capacity, k, out_idx,
-                                   static_cast<cudaStream_t>(stream));
+  cudaError_t e = qsa::launch_topk(logits, num_rows, row_stride, visible_cols, nullptr, 1, row_stride, max_visible, k,
+                                   out_idx, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(QSA_ERR_CUDA, "top-k launch: %s", cudaGetErrorString(e));
   return QSA_OK;
 }

@@ -53,10 +53,12 @@ cudaError_t fault_word_address(unsigned int** out);
 cudaError_t read_fault_word(uint32_t* flags, bool clear);
 // Top-k of every row over [0, n_r): n_r = visible[r] clamped to [0, min(capacity,
 // row_stride)], and 0 for a dead row (next_n_lens non-null: row r is dead when
-// r % rows_per_req >= next_n_lens[r / rows_per_req]).
+// r % rows_per_req >= next_n_lens[r / rows_per_req]).  max_visible > 0 is the
+// caller's bound on the n_r, a dispatch hint only: a row above it is still
+// selected exactly, more slowly.
 cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
-                        const int32_t* next_n_lens, int32_t rows_per_req, int64_t capacity, int32_t k,
-                        int32_t* out, cudaStream_t stream);
+                        const int32_t* next_n_lens, int32_t rows_per_req, int64_t capacity, int64_t max_visible,
+                        int32_t k, int32_t* out, cudaStream_t stream);
 
 // Cached per-device properties (queried once per device).
 struct DeviceInfo {

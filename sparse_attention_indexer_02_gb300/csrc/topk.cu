@@ -24,13 +24,11 @@ constexpr int kW = kT / 32;
 constexpr int kTn = 256;
 constexpr int64_t kNarrowSmem = 55 * 1024;
 // The register form: 1024 threads holding 8 keys each, one CTA an SM, for
-// launches of at most two rows an SM whose rows are bounded at kTr *
-// kRegKeysR columns (the capacity: the row stride, or a caller's bound; the
-// decode rows).  A row is one latency-bound chain on one SM (loads, digit
-// histograms, scans, stores); twice the threads halve each thread's part of
-// it (single-row decode top-k 5.78 -> 5.27 us against 512 threads of 16
-// keys).  Only the register path is reachable: the counts are clamped to the
-// bound, and the launch holds the three histograms alone.
+// launches of at most two rows an SM whose rows are at most kTr * kRegKeysR
+// columns (by the capacity, or by the caller's bound: the decode rows).  A
+// row is one latency-bound chain on one SM (loads, digit histograms, scans,
+// stores); twice the threads halve each thread's part of it (single-row
+// decode top-k 5.78 -> 5.27 us against 512 threads of 16 keys).
 constexpr int kTr = 1024;
 constexpr int kRegKeysR = 8;
 constexpr int64_t kSmemMax = 226 * 1024;  // dynamic shared memory per CTA (static part aside)
@@ -163,11 +161,13 @@ cudaError_t max_active_clusters(int c, size_t smem, int* out) {
   return cudaSuccess;
 }
 
-// The register form (kTr threads, kRegKeysR keys each): every row's count
-// is clamped to cap_cols <= kTr * kRegKeysR, so every row takes the register
-// path; the launch holds only its three histograms, with no cache, candidate
-// lists or pivot candidates (each sized 0: the other paths, never reached,
-// would stay inside the allocation).
+// The register form (kTr threads, kRegKeysR keys each): the launch holds
+// only the register path's three histograms, with no cache, candidate lists
+// or pivot candidates.  A row longer than kTr * kRegKeysR columns (a caller's
+// bound below its count) still selects exactly: the pivot is off (no
+// candidates), so it takes candidate compaction, whose lists of 0 entries
+// overflow at once, and which then reads its segment from global memory in
+// every pass, its one histogram at the start of the allocation.
 cudaError_t launch_register_form(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
                                  const int32_t* next_n_lens, int32_t rows_per_req, int64_t cap_cols, int32_t k,
                                  int32_t* out, unsigned int* fault, cudaStream_t stream) {
@@ -206,8 +206,8 @@ cudaError_t launch_register_form(const float* logits, int64_t num_rows, int64_t 
 }  // namespace
 
 cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_stride, const int32_t* visible,
-                        const int32_t* next_n_lens, int32_t rows_per_req, int64_t capacity, int32_t k,
-                        int32_t* out, cudaStream_t stream) {
+                        const int32_t* next_n_lens, int32_t rows_per_req, int64_t capacity, int64_t max_visible,
+                        int32_t k, int32_t* out, cudaStream_t stream) {
   if (num_rows == 0) return cudaSuccess;
   if (num_rows > 0x7FFFFFFFLL / kMaxCluster || row_stride > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   unsigned int* fault = nullptr;
@@ -216,10 +216,12 @@ cudaError_t launch_topk(const float* logits, int64_t num_rows, int64_t row_strid
   DeviceInfo dinfo;
   e = device_info(&dinfo);
   if (e != cudaSuccess) return e;
-  // Rows of at most kTr * kRegKeysR columns, few enough that each has an SM
-  // to itself or shares it with one other: the register form.
+  // Rows of at most kTr * kRegKeysR columns (by the capacity, or by the
+  // caller's bound), few enough that each has an SM to itself or shares it
+  // with one other: the register form.
   const int64_t cap_cols = capacity < row_stride ? capacity : row_stride;  // visible counts are clamped to it
-  if (cap_cols <= (int64_t)kTr * kRegKeysR && num_rows <= 2 * (int64_t)dinfo.num_sms)
+  const int64_t expect = max_visible > 0 && max_visible < cap_cols ? max_visible : cap_cols;
+  if (expect <= (int64_t)kTr * kRegKeysR && num_rows <= 2 * (int64_t)dinfo.num_sms)
     return launch_register_form(logits, num_rows, row_stride, visible, next_n_lens, rows_per_req, cap_cols, k, out,
                                 fault, stream);
   // Rows that may be longer than kSoloMax columns, and few enough that the

@@ -590,20 +590,39 @@ def test_bounded_topk_register_form_edge_rows(oracle_mod, k):
 
 @pytest.mark.parametrize("rows,width,bound", [(16, 65600, 8192), (40, 8192, 8192), (320, 4099, 5000),
                                               (3, 8191, 8191), (5, 1000, 700)])
-def test_bounded_topk_matches_oracle_with_counts_clamped(oracle_mod, rows, width, bound):
-    """Random rows whose counts reach past the bound (and past the stride):
-    the selection is the oracle's over min(visible, bound, width) columns.
-    The widths are not multiples of 4 except two (plain and vector loads);
-    320 rows is more than two an SM (152 SMs), which takes the general form."""
+def test_bounded_topk_rows_within_the_bound(oracle_mod, rows, width, bound):
+    """Random rows no longer than the bound (counts past the stride are
+    clamped to it): the widths are not multiples of 4 except two (plain and
+    vector loads); 320 rows is more than two an SM (152 SMs), which takes the
+    general form."""
     rng = np.random.default_rng(rows * 7 + width)
-    vis = rng.integers(0, int(bound * 1.3) + 2, size=rows).astype(np.int32)
-    vis[0] = bound + 5
-    vis[-1] = min(bound, width)
+    vis = rng.integers(0, min(bound, width) + 1, size=rows).astype(np.int32)
+    vis[0] = min(bound, width)
+    if width < bound:
+        vis[-1] = bound  # past the stride
     x = qi.random_logit_rows(rng, rows, width, np.minimum(vis, width), zero_frac=0.1)
     k = 2048 if bound > 2048 else 256
     idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k, max_visible=bound)
-    clamped = np.minimum(np.minimum(vis, bound), width).astype(np.int32)
-    assert_topk_strict(idx, oracle_mod.select_topk(x, clamped, k))
+    assert_topk_strict(idx, oracle_mod.select_topk(x, np.minimum(vis, width).astype(np.int32), k))
+
+
+@pytest.mark.parametrize("rows,width", [(16, 40003), (40, 12288)])
+def test_bounded_topk_rows_past_a_wrong_bound(oracle_mod, rows, width):
+    """A bound of 8192 columns that some rows exceed (up to 40,000 columns):
+    the register form's launch still selects them exactly (candidate
+    compaction from global memory).  Continuous values, then every row's
+    first-digit bin crowded (all values equal but a few)."""
+    rng = np.random.default_rng(rows + width)
+    vis = rng.integers(2000, width + 1, size=rows).astype(np.int32)
+    vis[0], vis[1], vis[2] = width, 8192, 8193
+    base = qi.random_logit_rows(rng, rows, width, vis, zero_frac=0.05)
+    flat = np.where(np.isfinite(base), np.float32(1.5), base)
+    flat[:, 5::997] = np.where(np.isfinite(flat[:, 5::997]), np.float32(2.0), flat[:, 5::997])
+    for x in (base, flat):
+        for k in (2048, 100):
+            idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k, max_visible=8192)
+            assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+    assert qsa.device_status() == 0
 
 
 def test_bounded_topk_key_spans_and_unaligned_rows(oracle_mod):
@@ -623,21 +642,18 @@ def test_bounded_topk_key_spans_and_unaligned_rows(oracle_mod):
         assert_topk_strict(idx, oracle_mod.select_topk(buf, vis, k))
 
 
-def test_bounded_topk_without_a_bound_is_the_plain_call():
-    """A bound of 0 (none), or one at or above the stride, gives exactly the
-    plain call's indices, as does a bound above 8192 (the general form)."""
+def test_bounded_topk_gives_the_plain_calls_indices_for_any_bound():
+    """The bound only chooses the launch: none (0, negative), at or above the
+    stride, above 8192 (the general form) or below the rows (the register
+    form) all give exactly the plain call's indices."""
     rng = np.random.default_rng(9)
     rows, width = 16, 20000
     vis = rng.integers(1000, width, size=rows).astype(np.int32)
     x = qi.random_logit_rows(rng, rows, width, vis, zero_frac=0.05)
     xt, vt = torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda()
     ref = gpu_topk(xt, vt, 2048)
-    for bound in (0, -3, width, width + 100, 12000):
-        got = gpu_topk(xt, vt, 2048, max_visible=bound)
-        if bound == 12000:
-            assert (got[vis <= 12000] == ref[vis <= 12000]).all()
-        else:
-            assert (got == ref).all()
+    for bound in (0, -3, width, width + 100, 12000, 8192, 3000):
+        assert (gpu_topk(xt, vt, 2048, max_visible=bound) == ref).all(), bound
     assert qsa.device_status() == 0
 
 
