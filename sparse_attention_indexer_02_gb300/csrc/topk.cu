@@ -28,7 +28,13 @@ constexpr int64_t kNarrowSmem = 55 * 1024;
 // columns (by the capacity, or by the caller's bound: the decode rows).  A
 // row is one latency-bound chain on one SM (loads, digit histograms, scans,
 // stores); twice the threads halve each thread's part of it (single-row
-// decode top-k 5.78 -> 5.27 us against 512 threads of 16 keys).
+// decode top-k 5.78 -> 5.27 us against 512 threads of 16 keys).  It is
+// compiled for two CTAs an SM (32 registers a thread, with a few spills that
+// cost it nothing measurable), so that it leaves half the register file to a
+// lean scoring CTA (256 threads of 128): the scoring launch that follows a
+// top-k then becomes resident on every SM while the top-k runs, instead of
+// starting its CTAs on the top-k's SMs only after it ends, with their 2.7 us
+// set-up exposed (decode step 16.6 -> 16.0 us).
 constexpr int kTr = 1024;
 constexpr int kRegKeysR = 8;
 constexpr int64_t kSmemMax = 226 * 1024;  // dynamic shared memory per CTA (static part aside)
@@ -51,7 +57,7 @@ struct TopkArgs {
 };
 
 template <bool CLUSTER, int NT>
-__global__ void __launch_bounds__(NT, NT == kTr ? 1 : (NT == kT ? 2 : 4)) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(NT, NT == kTn ? 4 : 2) topk_kernel(const TopkArgs a) {
   extern __shared__ uint4 dyn_topk[];
   __shared__ Shared sh;
   int CL = 1, rank = 0;  // cluster size and this CTA's rank in it
