@@ -625,6 +625,26 @@ def test_bounded_topk_rows_past_a_wrong_bound(oracle_mod, rows, width):
     assert qsa.device_status() == 0
 
 
+def test_bounded_topk_cluster_launch_with_a_wrong_bound(oracle_mod):
+    """Three rows of a 70,003-column stride under a bound of 16,000: a cluster
+    launch of 8 CTAs whose plan, going by the bound, has no segment cache.
+    Row 0 (70,003 columns, past the bound) takes candidate compaction from
+    global memory, row 1 (12,000) is selected by the first CTA alone (the
+    sampled pivot), row 2 (30,000) by the register path in every CTA.
+    Continuous values, then every row's first-digit bin crowded."""
+    rng = np.random.default_rng(70003)
+    width = 70003
+    vis = np.array([70003, 12000, 30000], np.int32)
+    base = qi.random_logit_rows(rng, 3, width, vis, zero_frac=0.05)
+    flat = np.where(np.isfinite(base), np.float32(1.5), base)
+    flat[:, 3::1001] = np.where(np.isfinite(flat[:, 3::1001]), np.float32(2.0), flat[:, 3::1001])
+    for x in (base, flat):
+        for k in (2048, 300):
+            idx = gpu_topk(torch.from_numpy(x).cuda(), torch.from_numpy(vis).cuda(), k, max_visible=16000)
+            assert_topk_strict(idx, oracle_mod.select_topk(x, vis, k))
+    assert qsa.device_status() == 0
+
+
 def test_bounded_topk_key_spans_and_unaligned_rows(oracle_mod):
     """The key-span rows under a bound of 8192 columns, with the logits
     starting one float past a 16-byte boundary and a stride of 8195 floats
