@@ -37,6 +37,17 @@ constexpr int64_t kNarrowSmem = 55 * 1024;
 // set-up exposed (decode step 16.6 -> 16.0 us).
 constexpr int kTr = 1024;
 constexpr int kRegKeysR = 8;
+// Its shared memory: the three histograms need 20 KB, but the launch takes
+// 116 KiB, so that two of its CTAs never share an SM (2 x (116 + 1 reserved)
+// KiB > 228 KiB) while a lean scoring CTA of the decode shapes (106 KB) still
+// fits beside one.  After a scoring form whose CTAs take whole SMs and leave
+// one by one (fp8 keys with bf16 q), a 20 KB launch put two rows on the first
+// SMs freed: a step of 16 rows of 8192 columns with 64 heads took 21.9 us,
+// against 19.4 us at 116 KiB (decode step unchanged, 16.3 us).
+constexpr size_t kRegFormSmem = 116 * 1024;
+constexpr size_t kSmPerSm = 228 * 1024;  // shared memory of an SM
+static_assert(2 * (kRegFormSmem + 1024) > kSmPerSm, "two register-form CTAs must not fit one SM");
+static_assert(kRegFormSmem >= 4 * (size_t)kRegHistWords, "the register path's histograms fit");
 constexpr int64_t kSmemMax = 226 * 1024;  // dynamic shared memory per CTA (static part aside)
 constexpr int kRegKeys = 16;              // keys per thread of the register path (rows <= 8192)
 
@@ -167,7 +178,7 @@ cudaError_t max_active_clusters(int c, size_t smem, int* out) {
   return cudaSuccess;
 }
 
-// The register form (kTr threads, kRegKeysR keys each): the launch holds
+// The register form (kTr threads, kRegKeysR keys each): the launch uses
 // only the register path's three histograms, with no cache, candidate lists
 // or pivot candidates.  A row longer than kTr * kRegKeysR columns (a caller's
 // bound below its count) still selects exactly: the pivot is off (no
@@ -191,7 +202,7 @@ cudaError_t launch_register_form(const float* logits, int64_t num_rows, int64_t 
   a.cpw = 0;
   a.pcap = 0;
   a.bulk = 0;
-  const size_t smem = 4 * (size_t)kRegHistWords;
+  const size_t smem = kRegFormSmem;
   cudaError_t e = cudaFuncSetAttribute(topk_kernel<false, kTr>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
