@@ -3,9 +3,9 @@
  * scoring and per-row top-k selection.
  *
  * The compute calls - scoring (qsa_paged_mqa_logits and its _ragged / _ex
- * forms), selection (qsa_select_topk) and both in one call
- * (qsa_paged_mqa_topk, qsa_paged_mqa_topk_noalloc) - follow the problem
- * statement of the pages:
+ * forms), selection (qsa_select_topk, qsa_select_topk_bounded) and both in
+ * one call (qsa_paged_mqa_topk, qsa_paged_mqa_topk_noalloc) - follow the
+ * problem statement of the pages:
  *   - vLLM #62589 "Tile QSA indexer scoring and skip invisible columns",
  *     Dispatch and Details: qsa_mqa_paged(...) scores request-major query rows
  *     against a paged compressed-key cache; top_k_per_row_decode reads
