@@ -43,7 +43,8 @@ constexpr int kRegKeysR = 8;
 // fits beside one.  After a scoring form whose CTAs take whole SMs and leave
 // one by one (fp8 keys with bf16 q), a 20 KB launch put two rows on the first
 // SMs freed: a step of 16 rows of 8192 columns with 64 heads took 21.9 us,
-// against 19.4 us at 116 KiB (decode step unchanged, 16.3 us).
+// against 19.4 us at 116 KiB (decode step unchanged, 16.3 us; tiny MTP
+// steps of 8 rows 8.85 -> 9.02 us).
 constexpr size_t kRegFormSmem = 116 * 1024;
 constexpr size_t kSmPerSm = 228 * 1024;  // shared memory of an SM
 static_assert(2 * (kRegFormSmem + 1024) > kSmPerSm, "two register-form CTAs must not fit one SM");
