@@ -28,10 +28,11 @@ constexpr int64_t kNarrowSmem = 55 * 1024;
 // columns (by the capacity, or by the caller's bound: the decode rows).  A
 // row is one latency-bound chain on one SM (loads, digit histograms, scans,
 // stores); twice the threads halve each thread's part of it (single-row
-// decode top-k 5.78 -> 5.27 us against 512 threads of 16 keys).  It is
-// compiled for two CTAs an SM (32 registers a thread, with a few spills that
-// cost it nothing measurable), so that it leaves half the register file to a
-// lean scoring CTA (256 threads of 128): the scoring launch that follows a
+// decode top-k 5.78 -> 5.27 us against 512 threads of 16 keys).  Its
+// registers are bounded as for two CTAs an SM (32 a thread, with a few
+// spills that cost it nothing measurable), so that it leaves half the
+// register file to a lean scoring CTA (256 threads of 128), while its shared
+// memory (below) keeps a second top-k CTA off the SM: the scoring launch that follows a
 // top-k then becomes resident on every SM while the top-k runs, instead of
 // starting its CTAs on the top-k's SMs only after it ends, with their 2.7 us
 // set-up exposed (decode step 16.6 -> 16.0 us).
