@@ -130,6 +130,23 @@ def test_caller_bound_steers_dispatch_only(oracle_mod, max_visible):
     assert workspace_is_zero()
 
 
+@pytest.mark.parametrize("vis,max_visible", [([9000, 16000, 30000, 100], 5000), ([8000, 100, 8192, 5000], 8192),
+                                              ([9000, 16000, 30000, 100], 30016)])
+def test_one_call_bound_chooses_the_topk_form_only(oracle_mod, vis, max_visible):
+    """With the automatic dispatch the one call runs the scoring and top-k
+    launches, and its bound picks the top-k form: the register form for a
+    bound of at most 8192 columns, whether right or wrong (rows of up to 30,000
+    columns under a bound of 5,000 are still selected exactly), the default
+    form above it."""
+    qsa.force_variant(qsa.VARIANT_AUTO)
+    case = ("bound_form", 4, 1, 4, 64, vis, 30016, 2048)
+    inp = qi.build_inputs(case_spec(case, qi.KV_BF16))
+    logits, idx, ran, _ = run_fused(inp, 2048, max_visible=max_visible)
+    assert ran == qsa.VARIANT_UMMA_LEAN
+    check(oracle_mod, inp, logits, idx, 2048, where=f"bound {max_visible}")
+    assert qsa.device_status() == 0
+
+
 def test_fused_rows_longer_than_the_shared_memory_cache(oracle_mod):
     """Columns past the selection's cache are read back from L2 by the fused kernel."""
     for kv_dtype, q_dtype in KINDS:
