@@ -775,8 +775,9 @@ def main(argv=None):
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the per-workload timings of the other configurations")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+    if args.warmup < 3:  # at least 3 warm-up steps; the JSON line reports the count used
+        print(f"bench: --warmup {args.warmup} raised to 3", file=sys.stderr)
+        args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)
