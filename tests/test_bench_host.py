@@ -36,3 +36,18 @@ def test_o0_record_reads_back(tmp_path, monkeypatch):
     assert qbuild.o0_units() == []
     rec.write_text('["umma_bf16"]')
     assert qbuild.o0_units() == ["umma_bf16"]
+
+
+def test_reference_arm_line_and_warmup_floor(capsys):
+    """The reference arm (the CPU oracle on a bounded sample) prints one JSON
+    line with the contract's keys; a warm-up below 3 steps runs as 3 and the
+    line reports 3."""
+    import json
+
+    bench.main(["--impl", "reference", "--steps", "1", "--warmup", "1", "--workload", "tiny_mtp"])
+    line = [x for x in capsys.readouterr().out.splitlines() if x.startswith("{")][-1]
+    d = json.loads(line)
+    assert d["impl"] == "reference" and d["warmup"] == 3 and d["steps"] == 1
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
